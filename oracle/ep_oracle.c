@@ -1,0 +1,424 @@
+/*
+ * CPU oracle for MoE token layout, dispatch and combine.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test-suite, the package smoke check and
+ * the CPU-baseline leg of the benchmark may load this file's library.  The
+ * product path (the CUDA library and its Python binding) never calls it.
+ *
+ * Plain, slow, scalar C11.  Every function follows the definition of the
+ * operation it computes, step by step, with no blocking, fusion or
+ * reordering.  It shares no code, header or constant table with the CUDA
+ * path.  Floating point: the method fixes fp32 (FP8 scale, quotient,
+ * identity-expert product, combine accumulation) and bf16 (payload, combine
+ * output); the oracle computes exactly those fp32 operations in the stated
+ * order.  Build with -ffp-contract=off so that no product and sum are fused.
+ *
+ * Source: ROCm MORI documentation, "Communication APIs" page, section
+ * "MORI-EP (Expert Parallelism)", table "EpDispatchCombineOp methods":
+ *   dispatch(input, weights, scales, indices)
+ *       -> (output, weights, scales, indices, recv_count)
+ *   combine(input, weights, indices) -> (output, weights)
+ *   get_dispatch_src_token_pos()
+ * and "Choosing an EP API and backend", "EPv2 configuration and lifecycle"
+ * (FP8 is OCP E4M3 on gfx950) and "Validation before tuning" (the
+ * identity-expert correctness check).
+ *
+ * Notation: W ranks, E experts, Er = E/W experts per rank, k = top-k,
+ * T = max tokens per rank, n_s = tokens present on source rank s (<= T),
+ * H = hidden size, cap = receive rows per rank.
+ * D(s,t) = { idx[s][t][j] / Er : j < k } (a set; duplicates collapse).
+ *
+ * Readings the pages leave open (taken as stated here):
+ *  - receive order on rank r is (source rank, then source token) ascending;
+ *  - src_pos of a received row is s*T + t;
+ *  - combine is an unweighted fp32 sum over r in D(s,t), r ascending,
+ *    started from +0.0f and rounded once to bf16; the returned weights are
+ *    the same ordered sum over the expert-side weight rows;
+ *  - carried weights / indices are all k entries, unchanged;
+ *  - FP8: per 128-element block a = max|x|, scale = fl(a/448),
+ *    q = E4M3_RNE_SATFINITE(fl(x/scale)); an all-zero block has scale 0 and
+ *    all codes 0x00; the sign of a zero code is kept otherwise;
+ *  - rows whose slot is >= cap are dropped by dispatch and skipped by
+ *    combine.
+ */
+#include <stdint.h>
+#include <string.h>
+#include <math.h>
+
+#define OR_OK 0
+#define OR_EINVAL 1
+
+/* ---------------------------------------------------------------- scalars */
+
+static float f32_from_bits(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+static uint32_t bits_from_f32(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+
+/* bf16 -> fp32 is exact: the bf16 pattern is the upper half of the fp32. */
+float or_bf16_to_f32(uint16_t b) { return f32_from_bits((uint32_t)b << 16); }
+
+/* fp32 -> bf16, round to nearest, ties to even (IEEE-754 roundTiesToEven).
+ * The kept part is the upper 16 bits; the discarded lower 16 bits decide:
+ * above one half ulp round up, below round down, exactly one half round to
+ * the even kept pattern.  A carry out of the mantissa moves to the next
+ * binade (or to infinity), which is the correct rounded value.  Inputs are
+ * finite in this method. */
+uint16_t or_bf16_rne(float f)
+{
+    uint32_t u = bits_from_f32(f);
+    uint32_t kept = u >> 16;
+    uint32_t rest = u & 0xFFFFu;
+    if (rest > 0x8000u || (rest == 0x8000u && (kept & 1u)))
+        kept += 1u;
+    return (uint16_t)kept;
+}
+
+/* Round a non-negative double to the nearest integer, ties to even. */
+static double round_half_even(double y)
+{
+    double f = floor(y);
+    double d = y - f;
+    if (d > 0.5) return f + 1.0;
+    if (d < 0.5) return f;
+    return (fmod(f, 2.0) == 0.0) ? f : f + 1.0;
+}
+
+/* OCP 8-bit floating point, E4M3 ("fn"): 1 sign bit, 4 exponent bits with
+ * bias 7, 3 mantissa bits.  Exponent field 0 holds subnormals m * 2^-9;
+ * fields 1..15 hold (1 + m/8) * 2^(e-7); S.1111.111 is NaN, so the largest
+ * finite magnitude is 1.75 * 2^8 = 448 (code 0x7E); there is no infinity.
+ * Encoding: round to nearest, ties to even mantissa; "satfinite" clamps
+ * magnitudes that round beyond 448 to 448.  The sign bit is always kept
+ * (so a negative value that rounds to zero gives 0x80).
+ *
+ * Codes are monotone in magnitude: with quantum 2^-9 below 2^-6 and
+ * 2^(e-3) in binade [2^e, 2^(e+1)), the code of n quanta is n in the
+ * subnormal range and (e+6)*8 + n in binade e (n in [8,16]); n = 16 lands
+ * on the first code of the next binade, which is the right rounding carry. */
+uint8_t or_e4m3_encode(float v)
+{
+    uint8_t sign = (bits_from_f32(v) >> 31) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    if (isnan(v)) return (uint8_t)(sign | 0x7F);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    int code;
+    if (a < ldexp(1.0, -6)) {
+        code = (int)round_half_even(a / ldexp(1.0, -9));      /* 0..8 */
+    } else {
+        int e2;
+        frexp(a, &e2);            /* a = m * 2^e2, m in [0.5, 1) */
+        int e = e2 - 1;           /* a in [2^e, 2^(e+1)), e in [-6, 8] */
+        int n = (int)round_half_even(a / ldexp(1.0, e - 3));  /* 8..16 */
+        code = (e + 6) * 8 + n;
+    }
+    if (code > 0x7E) code = 0x7E;  /* satfinite (a < 448 never exceeds it) */
+    return (uint8_t)(sign | code);
+}
+
+/* Value of an E4M3 code (exact in fp32). */
+float or_e4m3_value(uint8_t q)
+{
+    int s = q >> 7, e = (q >> 3) & 0xF, m = q & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return (float)(s ? -v : v);
+}
+
+/* One quantisation block of n bf16 values (n = 128 in this method):
+ * a = max |x_i| (exact), scale = fl32(a / 448), codes q_i =
+ * E4M3(fl32(x_i / scale)); a == 0 gives scale 0 and codes 0x00. */
+void or_quant_block(const uint16_t *x, int n, uint8_t *q, float *scale)
+{
+    float a = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float v = fabsf(or_bf16_to_f32(x[i]));
+        if (v > a) a = v;
+    }
+    if (a == 0.0f) {
+        *scale = 0.0f;
+        for (int i = 0; i < n; ++i) q[i] = 0x00;
+        return;
+    }
+    float s = a / 448.0f;
+    *scale = s;
+    for (int i = 0; i < n; ++i) {
+        float v = or_bf16_to_f32(x[i]) / s;
+        q[i] = or_e4m3_encode(v);
+    }
+}
+
+/* Element-wise forms of the scalars above, for testing over many values. */
+void or_bf16_rne_array(const float *v, uint16_t *o, int64_t n)
+{ for (int64_t i = 0; i < n; ++i) o[i] = or_bf16_rne(v[i]); }
+void or_e4m3_encode_array(const float *v, uint8_t *o, int64_t n)
+{ for (int64_t i = 0; i < n; ++i) o[i] = or_e4m3_encode(v[i]); }
+void or_e4m3_value_array(const uint8_t *q, float *o, int64_t n)
+{ for (int64_t i = 0; i < n; ++i) o[i] = or_e4m3_value(q[i]); }
+void or_quant_rows(const uint16_t *x, int64_t rows, int H, uint8_t *q, float *scales)
+{
+    for (int64_t i = 0; i < rows; ++i)
+        for (int b = 0; b < H / 128; ++b)
+            or_quant_block(x + i * H + b * 128, 128, q + i * H + b * 128,
+                           scales + i * (H / 128) + b);
+}
+
+/* ------------------------------------------------------------- validation */
+
+int or_validate(int W, int E, int k, int T, int H, int fp8,
+                const int32_t *idx, const int32_t *num_tokens)
+{
+    if (W < 1 || E < 1 || k < 1 || T < 0 || H < 1) return OR_EINVAL;
+    if (E % W != 0) return OR_EINVAL;
+    if (H % 8 != 0) return OR_EINVAL;
+    if (fp8 && H % 128 != 0) return OR_EINVAL;
+    for (int s = 0; s < W; ++s) {
+        if (num_tokens[s] < 0 || num_tokens[s] > T) return OR_EINVAL;
+        for (int t = 0; t < num_tokens[s]; ++t)
+            for (int j = 0; j < k; ++j) {
+                int32_t e = idx[((int64_t)s * T + t) * k + j];
+                if (e < 0 || e >= E) return OR_EINVAL;
+            }
+    }
+    return OR_OK;
+}
+
+/* ----------------------------------------------------------------- layout */
+
+/* Routing layout of one batch.
+ *   in_D[s][t][r]  = 1 iff r in D(s,t) and t < n_s
+ *   C[s][r]        = #{t < n_s : r in D(s,t)}            (send counts)
+ *   recv_count[r]  = sum_s C[s][r]
+ *   pos[s][t][r]   = sum_{s'<s} C[s'][r] + #{t' < t : r in D(s,t')}
+ *                    if r in D(s,t), else -1
+ * pos is int32 [W][T][W]; C is int32 [W][W]; recv_count int32 [W].
+ * in_D is caller scratch, uint8 [W][T][W]. */
+int or_layout(int W, int E, int k, int T, const int32_t *idx,
+              const int32_t *num_tokens, uint8_t *in_D,
+              int32_t *pos, int32_t *C, int32_t *recv_count)
+{
+    int Er = E / W;
+    memset(in_D, 0, (size_t)W * T * W);
+    for (int s = 0; s < W; ++s)
+        for (int t = 0; t < num_tokens[s]; ++t)
+            for (int j = 0; j < k; ++j) {
+                int r = idx[((int64_t)s * T + t) * k + j] / Er;
+                in_D[((int64_t)s * T + t) * W + r] = 1;
+            }
+    for (int s = 0; s < W; ++s)
+        for (int r = 0; r < W; ++r) {
+            int32_t c = 0;
+            for (int t = 0; t < T; ++t) c += in_D[((int64_t)s * T + t) * W + r];
+            C[s * W + r] = c;
+        }
+    for (int r = 0; r < W; ++r) {
+        int32_t tot = 0;
+        for (int s = 0; s < W; ++s) tot += C[s * W + r];
+        recv_count[r] = tot;
+    }
+    for (int s = 0; s < W; ++s)
+        for (int r = 0; r < W; ++r) {
+            int32_t base = 0;
+            for (int sp = 0; sp < s; ++sp) base += C[sp * W + r];
+            int32_t before = 0;   /* #{t' < t : r in D(s,t')} */
+            for (int t = 0; t < T; ++t) {
+                int64_t o = ((int64_t)s * T + t) * W + r;
+                if (in_D[o]) { pos[o] = base + before; before += 1; }
+                else pos[o] = -1;
+            }
+        }
+    return OR_OK;
+}
+
+/* --------------------------------------------------------------- dispatch */
+
+/* Dispatch, given the layout.  For every source token (s,t) with t < n_s and
+ * every r in D(s,t) with p = pos[s][t][r] < cap, row p of rank r receives:
+ *   out[r][p]        = x[s][t]                (bf16 bits), or the FP8 codes
+ *   out_scales[r][p] = the H/128 block scales (FP8 only)
+ *   out_w[r][p]      = w[s][t][0..k)
+ *   out_idx[r][p]    = idx[s][t][0..k)
+ *   src_pos[r][p]    = s*T + t
+ * Outputs are dense [W][cap][...]; rows never written are left as they are.
+ * out is uint16 [W][cap][H] for bf16, uint8 [W][cap][H] for FP8; with
+ * out == NULL only the per-row metadata (scales excepted) is produced. */
+int or_dispatch(int W, int k, int T, int H, int cap, int fp8,
+                const uint16_t *x, const float *w, const int32_t *idx,
+                const int32_t *num_tokens, const int32_t *pos,
+                void *out, float *out_scales, float *out_w,
+                int32_t *out_idx, int32_t *src_pos)
+{
+    int nb = fp8 ? H / 128 : 0;
+    for (int s = 0; s < W; ++s)
+        for (int t = 0; t < num_tokens[s]; ++t) {
+            const uint16_t *row = x + ((int64_t)s * T + t) * H;
+            for (int r = 0; r < W; ++r) {
+                int32_t p = pos[((int64_t)s * T + t) * W + r];
+                if (p < 0 || p >= cap) continue;
+                int64_t rp = (int64_t)r * cap + p;
+                if (!out) {
+                    /* metadata only */
+                } else if (fp8) {
+                    uint8_t *o = (uint8_t *)out + rp * H;
+                    for (int b = 0; b < nb; ++b)
+                        or_quant_block(row + b * 128, 128, o + b * 128,
+                                       out_scales + rp * nb + b);
+                } else {
+                    uint16_t *o = (uint16_t *)out + rp * H;
+                    for (int h = 0; h < H; ++h) o[h] = row[h];
+                }
+                for (int j = 0; j < k; ++j) {
+                    out_w[rp * k + j] = w[((int64_t)s * T + t) * k + j];
+                    out_idx[rp * k + j] = idx[((int64_t)s * T + t) * k + j];
+                }
+                src_pos[rp] = s * T + t;
+            }
+        }
+    return OR_OK;
+}
+
+/* Dispatched rows of a sample of receive slots: for i < n, (r, p) =
+ * (ranks[i], slots[i]) with p < min(recv_count[r], cap).  The source token
+ * of the slot is the unique (s,t) with pos[s][t][r] == p, found by scanning
+ * the layout; row i of the outputs is what dispatch writes to that slot
+ * (payload [n][H] as uint16 or uint8, scales [n][H/128], w and idx [n][k],
+ * src_pos [n]).  Returns OR_EINVAL if a slot has no source token. */
+int or_dispatch_rows(int W, int k, int T, int H, int fp8,
+                     const uint16_t *x, const float *w, const int32_t *idx,
+                     const int32_t *num_tokens, const int32_t *pos,
+                     const int32_t *ranks, const int32_t *slots, int n,
+                     void *out_rows, float *scale_rows, float *w_rows,
+                     int32_t *idx_rows, int32_t *src_rows)
+{
+    int nb = fp8 ? H / 128 : 0;
+    for (int i = 0; i < n; ++i) {
+        int r = ranks[i], found = 0;
+        for (int s = 0; s < W && !found; ++s)
+            for (int t = 0; t < num_tokens[s] && !found; ++t) {
+                if (pos[((int64_t)s * T + t) * W + r] != slots[i]) continue;
+                found = 1;
+                const uint16_t *row = x + ((int64_t)s * T + t) * H;
+                if (fp8) {
+                    for (int b = 0; b < nb; ++b)
+                        or_quant_block(row + b * 128, 128,
+                                       (uint8_t *)out_rows + (int64_t)i * H + b * 128,
+                                       scale_rows + (int64_t)i * nb + b);
+                } else {
+                    for (int h = 0; h < H; ++h)
+                        ((uint16_t *)out_rows)[(int64_t)i * H + h] = row[h];
+                }
+                for (int j = 0; j < k; ++j) {
+                    w_rows[(int64_t)i * k + j] = w[((int64_t)s * T + t) * k + j];
+                    idx_rows[(int64_t)i * k + j] = idx[((int64_t)s * T + t) * k + j];
+                }
+                src_rows[i] = s * T + t;
+            }
+        if (!found) return OR_EINVAL;
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------- identity expert */
+
+/* The identity expert of the benchmark's correctness check, on rank r:
+ * for each received row p < min(recv_count[r], cap),
+ *   alpha = +0.0f, then alpha = fl32(alpha + out_w[r][p][j]) for the j in
+ *           ascending order whose expert out_idx[r][p][j] lives on rank r;
+ *   v_h   = the bf16 payload as fp32, or fl32(value(q_h) * scale of its
+ *           block) for FP8;
+ *   y[r][p][h] = bf16_rne(fl32(v_h * alpha)).
+ * y is uint16 [W][cap][H]. */
+int or_identity_expert(int W, int E, int k, int H, int cap, int fp8,
+                       const int32_t *recv_count, const void *payload,
+                       const float *scales, const float *out_w,
+                       const int32_t *out_idx, uint16_t *y)
+{
+    int Er = E / W;
+    int nb = fp8 ? H / 128 : 0;
+    for (int r = 0; r < W; ++r) {
+        int n = recv_count[r] < cap ? recv_count[r] : cap;
+        for (int p = 0; p < n; ++p) {
+            int64_t rp = (int64_t)r * cap + p;
+            float alpha = 0.0f;
+            for (int j = 0; j < k; ++j)
+                if (out_idx[rp * k + j] / Er == r)
+                    alpha = alpha + out_w[rp * k + j];
+            for (int h = 0; h < H; ++h) {
+                float v;
+                if (fp8) {
+                    uint8_t q = ((const uint8_t *)payload)[rp * H + h];
+                    v = or_e4m3_value(q) * scales[rp * nb + h / 128];
+                } else {
+                    v = or_bf16_to_f32(((const uint16_t *)payload)[rp * H + h]);
+                }
+                float prod = v * alpha;
+                y[rp * H + h] = or_bf16_rne(prod);
+            }
+        }
+    }
+    return OR_OK;
+}
+
+/* ---------------------------------------------------------------- combine */
+
+/* Combine of one source token (s,t), given the layout:
+ *   acc_h = +0.0f; for r = 0..W-1 ascending with p = pos[s][t][r] in
+ *   [0, cap): acc_h = fl32(acc_h + fp32(y[r][p][h]));  out_h = bf16_rne(acc_h)
+ * and, if w_in is given, the same ordered fp32 sum of w_in[r][p][0..k)
+ * (no rounding at the end).  y is uint16 [W][cap][H], w_in float [W][cap][k].
+ */
+static void combine_token(int W, int k, int T, int H, int cap, int s, int t,
+                          const int32_t *pos, const uint16_t *y,
+                          const float *w_in, uint16_t *out_row, float *out_w_row)
+{
+    for (int h = 0; h < H; ++h) {
+        float acc = 0.0f;
+        for (int r = 0; r < W; ++r) {
+            int32_t p = pos[((int64_t)s * T + t) * W + r];
+            if (p < 0 || p >= cap) continue;
+            acc = acc + or_bf16_to_f32(y[((int64_t)r * cap + p) * H + h]);
+        }
+        out_row[h] = or_bf16_rne(acc);
+    }
+    if (w_in && out_w_row) {
+        for (int j = 0; j < k; ++j) {
+            float acc = 0.0f;
+            for (int r = 0; r < W; ++r) {
+                int32_t p = pos[((int64_t)s * T + t) * W + r];
+                if (p < 0 || p >= cap) continue;
+                acc = acc + w_in[((int64_t)r * cap + p) * k + j];
+            }
+            out_w_row[j] = acc;
+        }
+    }
+}
+
+/* Combine of every present token: out uint16 [W][T][H], out_w float
+ * [W][T][k] (nullable with w_in).  Rows t >= n_s are left as they are. */
+int or_combine(int W, int k, int T, int H, int cap, const int32_t *num_tokens,
+               const int32_t *pos, const uint16_t *y, const float *w_in,
+               uint16_t *out, float *out_w)
+{
+    for (int s = 0; s < W; ++s)
+        for (int t = 0; t < num_tokens[s]; ++t)
+            combine_token(W, k, T, H, cap, s, t, pos, y, w_in,
+                          out + ((int64_t)s * T + t) * H,
+                          out_w ? out_w + ((int64_t)s * T + t) * k : 0);
+    return OR_OK;
+}
+
+/* Combine of a sample of tokens, given as global ids g = s*T + t: row i of
+ * out_rows [n][H] (and out_w_rows [n][k]) is token tokens[i]. */
+int or_combine_tokens(int W, int k, int T, int H, int cap, const int32_t *pos,
+                      const uint16_t *y, const float *w_in,
+                      const int32_t *tokens, int n,
+                      uint16_t *out_rows, float *out_w_rows)
+{
+    for (int i = 0; i < n; ++i) {
+        int s = tokens[i] / T, t = tokens[i] % T;
+        combine_token(W, k, T, H, cap, s, t, pos, y, w_in,
+                      out_rows + (int64_t)i * H,
+                      out_w_rows ? out_w_rows + (int64_t)i * k : 0);
+    }
+    return OR_OK;
+}
