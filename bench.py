@@ -1,0 +1,484 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE EP hot path (layout + dispatch + combine) on GB300.
+
+One step = one pass of the whole path over one batch of the
+DeepSeek-V3-shaped workload (W=8 logical ranks, 256 experts, top-8,
+T=4096 tokens per rank, H=7168, bf16 payload, fp32-accumulate bf16
+combine): routing layout, dispatch send (copy of every token row to each of
+its destination ranks), dispatch receive (recv_count), combine (ordered fp32
+gather-reduce of the expert rows back to source order, weights included).
+The expert between dispatch and combine is outside the path: combine reads
+the registered combine buffer, filled once before timing by the identity
+expert of the correctness check.
+
+Prints ONE JSON line (rank 0).  `value` = tokens/s over all ranks (tokens =
+W*T per replica per step), device-timed with CUDA events; `e2e` = the same
+metric with the inputs copied from pinned host memory and the combined
+output copied back inside every step.  `--impl reference` times the CPU
+oracle (plain scalar C) on a bounded sample of the same workload instead.
+With torchrun (N>1) every rank runs an independent replica ("replicas
+only": the path has no exchange between GPUs on one device's segments).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine tokens/s and HBM GB/s (% of GB300 peak), 1 GPU"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = "dsv3"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------- bookkeeping
+
+def algorithmic_bytes(wl, P, N, fp8, with_weights=True):
+    """Bytes the method must move (each counted once).
+    dispatch: read N*(H*2 + 8k) [row once + ids + weights];
+              write P*(H*b + s_b + 8k + 4) [row, scales, weights, ids, src_pos]
+    combine:  read P*H*2 (+ P*4k weights); write N*H*2 (+ N*4k)."""
+    H, k = wl.hidden, wl.topk
+    b_out = 1 if fp8 else 2
+    s_b = 4 * (H // 128) if fp8 else 0
+    d_read = N * (H * 2 + 8 * k)
+    d_write = P * (H * b_out + s_b + 8 * k + 4)
+    c_read = P * H * 2 + (P * 4 * k if with_weights else 0)
+    c_write = N * H * 2 + (N * 4 * k if with_weights else 0)
+    return dict(dispatch=d_read + d_write, combine=c_read + c_write,
+                dispatch_read=d_read, dispatch_write=d_write,
+                combine_read=c_read, combine_write=c_write)
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "combine_ep_layout_06_gb300",
+                                          "csrc", "*")))
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[workload][kernel]
+        if e.get("src_sha") != kernel_source_sha():
+            return None
+        return float(e["bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons every 100 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100", "-i", str(index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            return
+        self.first = threading.Event()
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        self.first.wait(timeout=10)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+                self.first.set()
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if not self.samples:
+            return None
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = "during timed region"
+        if len(inside) < 2:
+            inside = [p for (_, p) in self.samples]
+            note = "whole run (timed region shorter than the sampling period)"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for p in inside if num(p[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for p in inside:
+            for n, v in zip(names, p[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(inside),
+                "window": note}
+
+
+# ------------------------------------------------------------ our path
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from combine_ep_layout_06_gb300 import inputs as gen
+    from combine_ep_layout_06_gb300.op import (EpDispatchCombineConfig,
+                                               EpDispatchCombineOp)
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = gen.WORKLOADS[args.workload]
+    W, T, H, k = wl.world_size, wl.max_tokens_per_rank, wl.hidden, wl.topk
+    inp = gen.make_inputs(wl)
+    N = W * T
+    Er = wl.experts_per_rank
+    P = int(sum(len(set((inp.indices[s, t] // Er).tolist()))
+                for s in range(W) for t in range(T)))
+
+    cfg = EpDispatchCombineConfig(W, wl.num_experts, k, H, T,
+                                  dispatch_dtype="fp8_e4m3" if wl.fp8 else "bf16")
+    op = EpDispatchCombineOp(cfg, device=dev)
+    x = torch.from_numpy(inp.x_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    w = torch.from_numpy(inp.weights).to(dev)
+    idx = torch.from_numpy(inp.indices).to(dev)
+    out = torch.empty((W, T, H), dtype=torch.bfloat16, device=dev)
+    out_w = torch.empty((W, T, k), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    nt = [T] * W
+
+    # identity expert fills the registered combine buffer (not timed) and
+    # the combined output must give back the input
+    with torch.cuda.stream(stream):
+        op.dispatch(x, w, None, idx, num_tokens=nt, stream=stream)
+        op.identity_expert(stream=stream)
+        op.combine(weights=op.out_w, out=out, out_weights=out_w, stream=stream)
+    stream.synchronize()
+    xs = x.float()
+    ys = out.float()
+    if wl.fp8:
+        ident_ok = bool(((ys - xs).abs() <= xs.abs() * 0.07 + 1e-2).all())
+    else:
+        ident_ok = bool(((ys - xs).abs() <= xs.abs() * (2.0 ** -8 * 10)).all())
+    st, mask = op.get_error(stream)
+    ident_ok = ident_ok and st == 0
+    del xs, ys
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        op.layout(idx, num_tokens=nt, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        op.dispatch_send_replay(x, w, idx, num_tokens=nt, stream=stream)
+        op.dispatch_recv(stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        op.combine(weights=op.out_w, out=out, out_weights=out_w, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+           for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        stop.record(stream)
+    stop.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_host1 = time.time()
+    total_ms = start.elapsed_time(stop)
+    lay = np.array([e[0].elapsed_time(e[1]) for e in evs])
+    dis = np.array([e[1].elapsed_time(e[2]) for e in evs])
+    com = np.array([e[2].elapsed_time(e[3]) for e in evs])
+    clocks = sampler.summary(t_host0, t_host1) if sampler else None
+    if sampler:
+        sampler.stop()
+    st, mask = op.get_error(stream)
+
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * N / (ms_per_step / 1e3)
+
+    ab = algorithmic_bytes(wl, P, N, wl.fp8)
+    step_bytes = ab["dispatch"] + ab["combine"]
+    peak, peak_kind = measured_peak()
+    d_ms, c_ms = float(dis.mean()), float(com.mean())
+    dominant = "combine" if c_ms >= d_ms else "dispatch"
+    dom_ms = c_ms if dominant == "combine" else d_ms
+    achieved = ab[dominant] / (dom_ms / 1e3) / 1e9
+    kname = "combine_kernel" if dominant == "combine" else "dispatch_kernel"
+
+    # end to end: pinned host inputs -> device, path, combined output -> host
+    e2e = None
+    if args.e2e_steps > 0:
+        hx = torch.from_numpy(inp.x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hw = torch.from_numpy(inp.weights).pin_memory()
+        hi = torch.from_numpy(inp.indices).pin_memory()
+        hout = torch.empty((W, T, H), dtype=torch.bfloat16).pin_memory()
+        dx, dw, di = torch.empty_like(x), torch.empty_like(w), torch.empty_like(idx)
+
+        def e2e_step():
+            dx.copy_(hx, non_blocking=True)
+            dw.copy_(hw, non_blocking=True)
+            di.copy_(hi, non_blocking=True)
+            op.dispatch(dx, dw, None, di, num_tokens=nt, stream=stream)
+            op.combine(weights=op.out_w, out=out, out_weights=out_w, stream=stream)
+            hout.copy_(out, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.e2e_steps):
+                e2e_step()
+            e1.record(stream)
+        e1.synchronize()
+        e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d = hx.numel() * 2 + hw.numel() * 4 + hi.numel() * 4
+        d2h = hout.numel() * 2
+        e2e = {"value": world * N / (e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, inp)
+
+    res = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8" if wl.fp8 else "bf16",
+        "data": "synthetic (seeded; shapes and routing of the workload, no dataset)",
+        "config": {
+            "workload": f"{wl.name}: W={W} logical ranks on one GPU, E={wl.num_experts}, "
+                        f"k={k}, T={T} tokens/rank, H={H}, "
+                        f"{'fp8 e4m3' if wl.fp8 else 'bf16'} dispatch, fp32-accumulate "
+                        f"bf16 combine with weights, {wl.routing} routing",
+            "tokens_per_step": N,
+            "routed_pairs": P,
+            "l2": "every input and output is larger than L2 (x 470 MB, "
+                  "dispatch out ~2.5 GB, combine in ~2.5 GB); no flush",
+            "parallelism": f"replicas x{world}",
+            "step": "layout + dispatch_send (routing replay of that layout) + "
+                    "dispatch_recv + combine, one stream",
+        },
+        "gb_per_s": step_bytes / (ms_per_step / 1e3) / 1e9,
+        "frac_of_nominal_8tbs": step_bytes / (ms_per_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+        "frac_of_measured_hbm": step_bytes / (ms_per_step / 1e3) / 1e9 / peak,
+        "algorithmic_bytes_per_step": int(step_bytes),
+        "layout_ms": float(lay.mean()),
+        "dispatch_ms": d_ms,
+        "combine_ms": c_ms,
+        "dispatch_gb_per_s": ab["dispatch"] / (d_ms / 1e3) / 1e9,
+        "combine_gb_per_s": ab["combine"] / (c_ms / 1e3) / 1e9,
+        "roofline": {
+            "bound": "hbm",
+            "kernel": kname,
+            "achieved": achieved,
+            "peak": peak,
+            "peak_kind": f"of {peak_kind} (hbm_gbs copy bandwidth)",
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": recorded_traffic(kname, wl.name),
+            "algorithmic_bytes_per_launch": int(ab[dominant]),
+        },
+        "identity_check": "pass" if ident_ok else "FAIL",
+        "device_errors": int(mask),
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    return res
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def cpu_baseline(wl, inp, repeats=1):
+    """The oracle as it stands (scalar C, one thread) on one batch of the
+    benchmark's own inputs (a bounded sample: one step's worth, about
+    5-15 s of CPU work): layout + dispatch + combine, the combine reading
+    the dispatched rows as the expert output."""
+    import oracle
+    swl = wl
+    cap = swl.world_size * swl.max_tokens_per_rank
+    sample_tokens = swl.max_tokens_per_rank
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        pos, C, rc = oracle.layout(swl, inp.indices, inp.num_tokens)
+        d = oracle.dispatch(swl, inp.x_bits, inp.weights, inp.indices,
+                            inp.num_tokens, pos, cap)
+        y = d["out"] if not swl.fp8 else np.zeros((swl.world_size, cap, swl.hidden), np.uint16)
+        oracle.combine(swl, inp.num_tokens, pos, y, d["out_w"], cap)
+        times.append(time.perf_counter() - t0)
+    tsec = float(np.median(times))
+    n = swl.world_size * swl.max_tokens_per_rank
+    return {"value": n / tsec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{wl.name} recipe at T={sample_tokens} tokens/rank "
+                      f"({n} tokens, H={swl.hidden}); layout+dispatch+combine; "
+                      f"{tsec:.2f} s wall, single thread",
+            "seconds": tsec}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle, timed per step on a bounded sample."""
+    import oracle
+    from combine_ep_layout_06_gb300 import inputs as gen
+    wl = gen.WORKLOADS[args.workload]
+    sample = 256
+    swl = wl.scaled(sample)
+    inp = gen.make_inputs(swl)
+    cap = swl.world_size * sample
+    n = swl.world_size * sample
+
+    def step():
+        pos, C, rc = oracle.layout(swl, inp.indices, inp.num_tokens)
+        d = oracle.dispatch(swl, inp.x_bits, inp.weights, inp.indices,
+                            inp.num_tokens, pos, cap)
+        y = d["out"] if not swl.fp8 else np.zeros((swl.world_size, cap, swl.hidden), np.uint16)
+        oracle.combine(swl, inp.num_tokens, pos, y, d["out_w"], cap)
+
+    for _ in range(args.warmup):
+        step()
+    steps = max(1, args.steps)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    tsec = (time.perf_counter() - t0) / steps
+    v = n / tsec
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": tsec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8" if wl.fp8 else "bf16", "data": "synthetic",
+        "config": {"workload": f"{wl.name} recipe, oracle sample of {sample} "
+                               f"tokens/rank ({n} tokens) per step"},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1,
+                         "kind": "oracle",
+                         "sample": f"{n} tokens of the {wl.name} recipe per step"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

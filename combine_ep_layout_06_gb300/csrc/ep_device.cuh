@@ -1,0 +1,82 @@
+// Device-side helpers: cache-hinted 16/8-byte memory ops, release/acquire
+// flag ops, a bounded wait and the sticky error word.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ep_internal.cuh"
+
+namespace ep {
+
+// Streaming read of data used once (not allocated in L1).
+__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Streaming (evict-first) stores.
+__device__ __forceinline__ void st_stream16(void *p, const uint4 &v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_stream8(void *p, const uint2 &v) {
+    asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};"
+                 :: "l"(p), "r"(v.x), "r"(v.y)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v)
+                 : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p,
+                                                         uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;"
+                 : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+__device__ __forceinline__ void set_error(uint32_t *words, uint32_t bit) {
+    atomicOr(words + kWordErr, bit);
+}
+
+// Spin until *p == want, for at most timeout_ns of %globaltimer and at most
+// a fixed number of polls.  Returns false on expiry (the caller records
+// EP_DEVERR_TIMEOUT).  Never waits without a bound.
+__device__ __forceinline__ bool wait_flag_eq(const uint32_t *p, uint32_t want,
+                                             int64_t timeout_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    const uint32_t max_polls = 1u << 24;
+    for (uint32_t it = 0;; ++it) {
+        if (ld_acquire_gpu(p) == want) return true;
+        if (it >= max_polls) return false;
+        if ((int64_t)(globaltimer_ns() - t0) > timeout_ns) return false;
+        __nanosleep(128);
+    }
+}
+
+}  // namespace ep

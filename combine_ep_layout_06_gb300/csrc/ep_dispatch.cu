@@ -1,0 +1,290 @@
+// Dispatch copy: every present token row goes, once per distinct destination
+// rank, to its receive slot in that rank's segment, with its k weights, k
+// expert ids and its source position; optionally the row is quantised to
+// OCP FP8 E4M3 with one fp32 scale per 128 elements on the way.
+//
+// Definition (ROCm MORI "Communication APIs", MORI-EP, "EpDispatchCombineOp
+// methods": dispatch(input, weights, scales, indices) -> (output, weights,
+// scales, indices, recv_count); get_dispatch_src_token_pos()).  FP8 is OCP
+// E4M3 ("EPv2 configuration and lifecycle"); per block a = max|x|,
+// scale = fl32(a/448), q = RNE-satfinite(fl32(x/scale)), a == 0 -> scale 0,
+// codes 0.
+//
+// GB300 mapping.  One CTA per 32-token layout chunk.  Warp 0 turns the
+// chunk's masks and the chunk bases into receive slots (ballot + popc of the
+// lanes below) and writes pos; then each warp streams whole token rows: the
+// source row is read ONCE from HBM (16-byte non-allocating loads, U vectors
+// in flight per lane) and stored to each destination row with 16-byte
+// evict-first stores, 512 contiguous bytes per warp instruction.
+#include <cuda_fp8.h>
+
+#include "ep_device.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kDispatchWarps = 4;
+constexpr int kDispatchThreads = kDispatchWarps * 32;
+constexpr int kMaxFp8Blocks = 128;   // H <= 16384 for FP8
+
+struct DispatchParams {
+    const uint4 *x;
+    const float *w;
+    const int32_t *idx;
+    const uint32_t *masks;
+    const int32_t *chunk_base;
+    int32_t *pos;
+    char *seg0;
+    int64_t seg_stride, off_out, off_scales, off_w, off_idx, off_src;
+    uint32_t *words;
+    uint32_t *dflags;
+    int W, k, T, H, nch, cap, nvec, nb;
+    int notify;
+    uint32_t epoch;
+    TokenCounts nt;
+};
+
+struct DispatchSmem {
+    int32_t pos[kChunk][EP_MAX_WORLD];
+    uint32_t mask[kChunk];
+    float scales[kDispatchWarps][kMaxFp8Blocks];
+};
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float f[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// 8 values -> 8 E4M3 codes (byte i = element i) given the block scale.
+__device__ __forceinline__ uint2 quant8(const float f[8], float scale) {
+    uint32_t word[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t packed = 0;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float a = f[4 * h + 2 * i] / scale;
+            const float b = f[4 * h + 2 * i + 1] / scale;
+            const __nv_fp8x2_storage_t q =
+                __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+            packed |= (uint32_t)q << (16 * i);
+        }
+        word[h] = packed;
+    }
+    return make_uint2(word[0], word[1]);
+}
+
+template <bool FP8, int U>
+__global__ void __launch_bounds__(kDispatchThreads)
+dispatch_kernel(const DispatchParams p) {
+    __shared__ DispatchSmem sm;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int g = blockIdx.x;
+    const int s = g / p.nch;
+    const int t0 = (g - s * p.nch) * kChunk;
+    const int n_s = p.nt.n[s];
+
+    // ---- receive slots of the chunk's tokens (layout, within-chunk part)
+    if (warp == 0) {
+        const int t = t0 + lane;
+        const uint32_t m = (t < n_s) ? p.masks[(int64_t)s * p.T + t] : 0u;
+        const int my_base = (lane < p.W) ? p.chunk_base[(int64_t)g * p.W + lane] : 0;
+        const uint32_t below = lanemask_lt();
+        for (int r = 0; r < p.W; ++r) {
+            const uint32_t b = __ballot_sync(0xffffffffu, (m >> r) & 1u);
+            const int base = __shfl_sync(0xffffffffu, my_base, r);
+            sm.pos[lane][r] = ((m >> r) & 1u) ? base + __popc(b & below) : -1;
+        }
+        sm.mask[lane] = m;
+        if (t < p.T) {
+            int32_t *dst = p.pos + ((int64_t)s * p.T + t) * p.W;
+            for (int r = 0; r < p.W; ++r) dst[r] = sm.pos[lane][r];
+        }
+    }
+    __syncthreads();
+
+    // ---- rows
+    for (int i = warp; i < kChunk; i += kDispatchWarps) {
+        const int t = t0 + i;
+        if (t >= n_s) break;
+        const uint32_t m = sm.mask[i];
+        if (m == 0u) continue;
+        const int64_t tok = (int64_t)s * p.T + t;
+
+        // metadata: all k weights, all k ids, src_pos
+        float wv = 0.f;
+        int32_t iv = 0;
+        if (lane < p.k) {
+            wv = __ldg(p.w + tok * p.k + lane);
+            iv = __ldg(p.idx + tok * p.k + lane);
+        }
+        for (uint32_t mm = m; mm; mm &= mm - 1u) {
+            const int r = __ffs(mm) - 1;
+            const int slot = sm.pos[i][r];
+            if (slot >= p.cap) continue;
+            char *seg = p.seg0 + (int64_t)r * p.seg_stride;
+            if (lane < p.k) {
+                reinterpret_cast<float *>(seg + p.off_w)[(int64_t)slot * p.k + lane] = wv;
+                reinterpret_cast<int32_t *>(seg + p.off_idx)[(int64_t)slot * p.k + lane] = iv;
+            }
+            if (lane == 0)
+                reinterpret_cast<int32_t *>(seg + p.off_src)[slot] = (int32_t)(s * p.T + t);
+        }
+
+        // payload
+        const uint4 *src = p.x + tok * p.nvec;
+        for (int v0 = lane; v0 < p.nvec; v0 += 32 * U) {
+            if constexpr (!FP8) {
+                uint4 buf[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int v = v0 + 32 * u;
+                    if (v < p.nvec) buf[u] = ld_stream16(src + v);
+                }
+                for (uint32_t mm = m; mm; mm &= mm - 1u) {
+                    const int r = __ffs(mm) - 1;
+                    const int slot = sm.pos[i][r];
+                    if (slot >= p.cap) continue;
+                    uint4 *dst = reinterpret_cast<uint4 *>(
+                                     p.seg0 + (int64_t)r * p.seg_stride + p.off_out) +
+                                 (int64_t)slot * p.nvec;
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int v = v0 + 32 * u;
+                        if (v < p.nvec) st_stream16(dst + v, buf[u]);
+                    }
+                }
+            } else {
+                uint2 q[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int v = v0 + 32 * u;
+                    const bool active = v < p.nvec;   // whole half-warps
+                    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+                    if (active) raw = ld_stream16(src + v);
+                    float f[8];
+                    unpack_bf16x8(raw, f);
+                    float a = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(f[e]));
+#pragma unroll
+                    for (int o = 8; o > 0; o >>= 1)
+                        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+                    float scale = 0.f;
+                    q[u] = make_uint2(0u, 0u);
+                    if (a != 0.f) {
+                        scale = a / 448.0f;
+                        q[u] = quant8(f, scale);
+                    }
+                    if (active && (lane & 15) == 0) sm.scales[warp][v >> 4] = scale;
+                }
+                for (uint32_t mm = m; mm; mm &= mm - 1u) {
+                    const int r = __ffs(mm) - 1;
+                    const int slot = sm.pos[i][r];
+                    if (slot >= p.cap) continue;
+                    char *dst = p.seg0 + (int64_t)r * p.seg_stride + p.off_out +
+                                (int64_t)slot * p.H;
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int v = v0 + 32 * u;
+                        if (v < p.nvec) st_stream8(dst + (int64_t)v * 8, q[u]);
+                    }
+                }
+            }
+        }
+        if constexpr (FP8) {
+            __syncwarp();
+            for (uint32_t mm = m; mm; mm &= mm - 1u) {
+                const int r = __ffs(mm) - 1;
+                const int slot = sm.pos[i][r];
+                if (slot >= p.cap) continue;
+                float *dst = reinterpret_cast<float *>(
+                                 p.seg0 + (int64_t)r * p.seg_stride + p.off_scales) +
+                             (int64_t)slot * p.nb;
+                for (int b = lane; b < p.nb; b += 32) dst[b] = sm.scales[warp][b];
+            }
+            __syncwarp();
+        }
+    }
+
+    // ---- ready notification: the last CTA of source s posts (s -> r) for
+    // every r, zero-count pairs included, after all of s's rows are stored.
+    if (p.notify) {
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const uint32_t tk = atom_add_acq_rel_gpu(p.words + kWordSrcDone + s, 1u);
+            if (tk == (uint32_t)p.nch - 1u) {
+                p.words[kWordSrcDone + s] = 0u;
+                for (int r = 0; r < p.W; ++r)
+                    st_release_gpu(p.dflags + r * p.W + s, p.epoch);
+            }
+        }
+    }
+}
+
+__global__ void dispatch_recv_kernel(uint32_t *dflags, uint32_t *words,
+                                     const int32_t *totals, int32_t *recv_count,
+                                     int W, int check, uint32_t epoch,
+                                     int64_t timeout_ns) {
+    const int tid = threadIdx.x;
+    if (check && tid < W * W) {
+        if (!wait_flag_eq(dflags + tid, epoch, timeout_ns))
+            set_error(words, EP_DEVERR_TIMEOUT);
+    }
+    __syncthreads();
+    if (tid < W) recv_count[tid] = totals[tid];
+}
+
+template <bool FP8, int U>
+cudaError_t launch_dispatch_t(const Config &c, const DispatchParams &p,
+                              cudaStream_t st) {
+    dispatch_kernel<FP8, U><<<c.G, kDispatchThreads, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const Config &c, const Workspace &ws,
+                            const DispatchArgs &a, cudaStream_t st) {
+    DispatchParams p;
+    p.x = reinterpret_cast<const uint4 *>(a.x);
+    p.w = a.w;
+    p.idx = a.idx;
+    p.masks = ws.masks;
+    p.chunk_base = ws.chunk_base;
+    p.pos = ws.pos;
+    p.seg0 = ws.seg0;
+    p.seg_stride = ws.seg_stride;
+    p.off_out = ws.off_out;
+    p.off_scales = ws.off_scales;
+    p.off_w = ws.off_w;
+    p.off_idx = ws.off_idx;
+    p.off_src = ws.off_src;
+    p.words = ws.words;
+    p.dflags = ws.dflags;
+    p.W = c.W; p.k = c.k; p.T = c.T; p.H = c.H; p.nch = c.nch; p.cap = c.cap;
+    p.nvec = c.nvec; p.nb = c.nb;
+    p.notify = c.early_notify ? 1 : 0;
+    p.epoch = a.epoch;
+    p.nt = a.nt;
+    if (c.fp8) return launch_dispatch_t<true, 4>(c, p, st);
+    return launch_dispatch_t<false, 4>(c, p, st);
+}
+
+cudaError_t launch_dispatch_recv(const Config &c, const Workspace &ws,
+                                 bool check_flags, uint32_t epoch,
+                                 cudaStream_t st) {
+    const int threads = ((c.W * c.W + 31) / 32) * 32;
+    dispatch_recv_kernel<<<1, threads, 0, st>>>(
+        ws.dflags, ws.words, ws.chunk_base + (int64_t)c.G * c.W, ws.recv_count,
+        c.W, check_flags ? 1 : 0, epoch, c.timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace ep

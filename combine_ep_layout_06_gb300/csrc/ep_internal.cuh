@@ -1,0 +1,121 @@
+// Internal definitions shared by the CUDA translation units of the library:
+// the handle, the workspace map and the kernel launch wrappers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ep_api.h"
+
+namespace ep {
+
+// Tokens per layout chunk: one warp ballots over 32 tokens, so a chunk's
+// per-destination counts come from one __ballot_sync + __popc each.
+constexpr int kChunk = 32;
+
+// Offsets of the small counters at the start of the workspace (u32 words).
+constexpr int kWordErr = 0;        // sticky device error word
+constexpr int kWordLayoutDone = 1; // "last CTA" ticket of the layout kernel
+constexpr int kWordSrcDone = 8;    // [W] per-source ticket of the dispatch copy
+constexpr int kCounterWords = 64;  // 256 bytes
+
+struct Workspace {
+    // layout state
+    uint32_t *words;       // kCounterWords u32
+    uint32_t *dflags;      // [W dst][W src]
+    uint32_t *cflags;      // [W src][W dst]
+    int32_t *chunk_cnt;    // [G][W]   per-chunk destination counts
+    int32_t *chunk_base;   // [G+1][W] exclusive prefix over chunks; row G = totals
+    int32_t *send_counts;  // [W][W]
+    int32_t *recv_count;   // [W] published by the receive step
+    uint32_t *masks;       // [W][T]   destination-rank bit mask per token
+    int32_t *pos;          // [W][T][W]
+    // rank-0 segment; rank r's copy is at + r * seg_stride bytes
+    char *seg0;
+    int64_t seg_stride;
+    int64_t off_out, off_scales, off_w, off_idx, off_src, off_comb;
+    size_t total_bytes;
+};
+
+struct Config {
+    int W, E, Er, k, H, T, cap;
+    bool fp8;
+    int nch;     // chunks per source rank = ceil(T / kChunk)
+    int G;       // W * nch
+    int nvec;    // 16-byte vectors per bf16 row = H / 8
+    int nb;      // FP8 blocks per row = H / 128 (0 for bf16)
+    bool early_notify, fused_recv;
+    int64_t timeout_ns;
+};
+
+// Plan the workspace of a config; base may be null (sizing only).
+void plan_workspace(const Config &c, char *base, Workspace *ws);
+
+// Per-call token counts, passed by value to kernels.
+struct TokenCounts {
+    int32_t n[EP_MAX_WORLD];
+};
+
+// ---------------------------------------------------------------- kernels
+// Each launcher enqueues on `st` and returns cudaGetLastError().
+
+// publish: also write recv_count (when no separate receive step follows).
+cudaError_t launch_layout(const Config &c, const Workspace &ws,
+                          const int32_t *idx, const TokenCounts &nt,
+                          cudaStream_t st, bool publish);
+
+struct DispatchArgs {
+    const void *x;         // [W][T][H] bf16
+    const float *w;        // [W][T][k]
+    const int32_t *idx;    // [W][T][k]
+    TokenCounts nt;
+    uint32_t epoch;        // flag value when early_notify
+};
+cudaError_t launch_dispatch(const Config &c, const Workspace &ws,
+                            const DispatchArgs &a, cudaStream_t st);
+
+// Receive step: optional bounded flag check, then publish recv_count.
+cudaError_t launch_dispatch_recv(const Config &c, const Workspace &ws,
+                                 bool check_flags, uint32_t epoch,
+                                 cudaStream_t st);
+
+cudaError_t launch_combine_notify(const Config &c, const Workspace &ws,
+                                  uint32_t epoch, cudaStream_t st);
+cudaError_t launch_combine_wait(const Config &c, const Workspace &ws,
+                                uint32_t epoch, cudaStream_t st);
+
+struct CombineArgs {
+    const char *y;          // rank 0 rows; rank r at + r*y_stride
+    int64_t y_stride;
+    const char *w_in;       // nullable
+    int64_t w_stride;
+    const int32_t *idx;     // nullable
+    uint16_t *out;          // [W][T][H]
+    float *out_w;           // nullable
+    TokenCounts nt;
+    bool fused_wait;        // fused receive: each CTA waits on the flags
+    uint32_t epoch;
+};
+cudaError_t launch_combine(const Config &c, const Workspace &ws,
+                           const CombineArgs &a, cudaStream_t st);
+
+cudaError_t launch_identity_expert(const Config &c, const Workspace &ws,
+                                   char *y, int64_t y_stride, cudaStream_t st);
+
+}  // namespace ep
+
+// Host handle.
+struct ep_handle {
+    ep::Config cfg;
+    ep::Workspace ws;
+    int device;
+    cudaEvent_t ev_dispatch_sent;
+    cudaEvent_t ev_combine_sent;
+    uint32_t dispatch_epoch;
+    uint32_t combine_epoch;
+    bool layout_valid;      // a layout exists for combine / replay
+    bool dispatch_pending;  // sent, not yet received
+    bool combine_pending;   // combine sent, not yet received
+    ep::TokenCounts layout_nt;
+    int log_level;
+};

@@ -74,6 +74,9 @@ def _declare(L):
                                   _P, _P, _I, _P, _P, _P, _P, _P]),
         "or_identity_expert": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
                                     _P, _P]),
+        "or_identity_rows": (_I, [_I, _I, _I, _I, _I, _P, _I, _P, _P, _P,
+                                  _P, _P]),
+        "or_combine_gathered": (_I, [_I, _I, _P, _P]),
         "or_combine": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
         "or_combine_tokens": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _I,
                                    _P, _P]),
@@ -229,6 +232,32 @@ def identity_expert(wl, recv_count, payload, scales, out_w, out_idx, cap,
                              _p(_c(out_w, np.float32)),
                              _p(_c(out_idx, np.int32)), _p(y))
     return y
+
+
+def identity_rows(wl, ranks, payload, scales, w, idx, fp8=None):
+    """Identity-expert output of listed rows (row i received on ranks[i])."""
+    fp8 = wl.fp8 if fp8 is None else fp8
+    ranks = _c(ranks, np.int32)
+    n = ranks.size
+    H = wl.hidden
+    y = np.zeros((n, H), np.uint16)
+    sc = (_c(scales, np.float32) if fp8 else np.zeros((n, 1), np.float32))
+    lib().or_identity_rows(wl.world_size, wl.num_experts, wl.topk, H, int(fp8),
+                           _p(ranks), n,
+                           _p(_c(payload, np.uint8 if fp8 else np.uint16)),
+                           _p(sc), _p(_c(w, np.float32)), _p(_c(idx, np.int32)),
+                           _p(y))
+    return y
+
+
+def combine_gathered(rows):
+    """Combine sum of one token's rows [nd][H] given in ascending rank order."""
+    rows = _c(rows, np.uint16)
+    nd, H = rows.shape
+    out = np.zeros(H, np.uint16)
+    if lib().or_combine_gathered(nd, H, _p(rows), _p(out)) != 0:
+        raise OracleError("too many rows")
+    return out
 
 
 def combine(wl, num_tokens, pos, y, w_in, cap):

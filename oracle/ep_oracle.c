@@ -168,7 +168,7 @@ void or_quant_rows(const uint16_t *x, int64_t rows, int H, uint8_t *q, float *sc
 int or_validate(int W, int E, int k, int T, int H, int fp8,
                 const int32_t *idx, const int32_t *num_tokens)
 {
-    if (W < 1 || E < 1 || k < 1 || T < 0 || H < 1) return OR_EINVAL;
+    if (W < 1 || W > 64 || E < 1 || k < 1 || T < 0 || H < 1) return OR_EINVAL;
     if (E % W != 0) return OR_EINVAL;
     if (H % 8 != 0) return OR_EINVAL;
     if (fp8 && H % 128 != 0) return OR_EINVAL;
@@ -320,14 +320,34 @@ int or_dispatch_rows(int W, int k, int T, int H, int fp8,
 
 /* ------------------------------------------------------- identity expert */
 
-/* The identity expert of the benchmark's correctness check, on rank r:
- * for each received row p < min(recv_count[r], cap),
- *   alpha = +0.0f, then alpha = fl32(alpha + out_w[r][p][j]) for the j in
- *           ascending order whose expert out_idx[r][p][j] lives on rank r;
+/* The identity expert of the benchmark's correctness check, for one row
+ * received on rank r:
+ *   alpha = +0.0f, then alpha = fl32(alpha + w[j]) for the j in ascending
+ *           order whose expert idx[j] lives on rank r;
  *   v_h   = the bf16 payload as fp32, or fl32(value(q_h) * scale of its
  *           block) for FP8;
- *   y[r][p][h] = bf16_rne(fl32(v_h * alpha)).
- * y is uint16 [W][cap][H]. */
+ *   y[h]  = bf16_rne(fl32(v_h * alpha)). */
+static void identity_row(int r, int Er, int k, int H, int fp8,
+                         const void *payload, const float *scales,
+                         const float *w, const int32_t *idx, uint16_t *y)
+{
+    float alpha = 0.0f;
+    for (int j = 0; j < k; ++j)
+        if (idx[j] / Er == r)
+            alpha = alpha + w[j];
+    for (int h = 0; h < H; ++h) {
+        float v;
+        if (fp8)
+            v = or_e4m3_value(((const uint8_t *)payload)[h]) * scales[h / 128];
+        else
+            v = or_bf16_to_f32(((const uint16_t *)payload)[h]);
+        float prod = v * alpha;
+        y[h] = or_bf16_rne(prod);
+    }
+}
+
+/* Identity expert over whole receive buffers: every received row
+ * p < min(recv_count[r], cap) of every rank r.  y is uint16 [W][cap][H]. */
 int or_identity_expert(int W, int E, int k, int H, int cap, int fp8,
                        const int32_t *recv_count, const void *payload,
                        const float *scales, const float *out_w,
@@ -339,47 +359,64 @@ int or_identity_expert(int W, int E, int k, int H, int cap, int fp8,
         int n = recv_count[r] < cap ? recv_count[r] : cap;
         for (int p = 0; p < n; ++p) {
             int64_t rp = (int64_t)r * cap + p;
-            float alpha = 0.0f;
-            for (int j = 0; j < k; ++j)
-                if (out_idx[rp * k + j] / Er == r)
-                    alpha = alpha + out_w[rp * k + j];
-            for (int h = 0; h < H; ++h) {
-                float v;
-                if (fp8) {
-                    uint8_t q = ((const uint8_t *)payload)[rp * H + h];
-                    v = or_e4m3_value(q) * scales[rp * nb + h / 128];
-                } else {
-                    v = or_bf16_to_f32(((const uint16_t *)payload)[rp * H + h]);
-                }
-                float prod = v * alpha;
-                y[rp * H + h] = or_bf16_rne(prod);
-            }
+            const void *row = fp8 ? (const void *)((const uint8_t *)payload + rp * H)
+                                  : (const void *)((const uint16_t *)payload + rp * H);
+            identity_row(r, Er, k, H, fp8, row, fp8 ? scales + rp * nb : 0,
+                         out_w + rp * k, out_idx + rp * k, y + rp * H);
         }
+    }
+    return OR_OK;
+}
+
+/* Identity expert of n listed rows: row i was received on rank ranks[i];
+ * payload [n][H] (uint16 or uint8), scales [n][H/128], w and idx [n][k]. */
+int or_identity_rows(int W, int E, int k, int H, int fp8, const int32_t *ranks,
+                     int n, const void *payload, const float *scales,
+                     const float *w, const int32_t *idx, uint16_t *y)
+{
+    int Er = E / W;
+    int nb = fp8 ? H / 128 : 0;
+    for (int i = 0; i < n; ++i) {
+        const void *row = fp8 ? (const void *)((const uint8_t *)payload + (int64_t)i * H)
+                              : (const void *)((const uint16_t *)payload + (int64_t)i * H);
+        identity_row(ranks[i], Er, k, H, fp8, row, fp8 ? scales + (int64_t)i * nb : 0,
+                     w + (int64_t)i * k, idx + (int64_t)i * k, y + (int64_t)i * H);
     }
     return OR_OK;
 }
 
 /* ---------------------------------------------------------------- combine */
 
-/* Combine of one source token (s,t), given the layout:
- *   acc_h = +0.0f; for r = 0..W-1 ascending with p = pos[s][t][r] in
- *   [0, cap): acc_h = fl32(acc_h + fp32(y[r][p][h]));  out_h = bf16_rne(acc_h)
- * and, if w_in is given, the same ordered fp32 sum of w_in[r][p][0..k)
- * (no rounding at the end).  y is uint16 [W][cap][H], w_in float [W][cap][k].
- */
+/* The combine sum of one token from its rows in ascending rank order:
+ *   acc_h = +0.0f; acc_h = fl32(acc_h + fp32(rows[i][h])) for i = 0..nd-1;
+ *   out_h = bf16_rne(acc_h). */
+static void sum_rows(int nd, const uint16_t *const *rows, int H, uint16_t *out)
+{
+    for (int h = 0; h < H; ++h) {
+        float acc = 0.0f;
+        for (int i = 0; i < nd; ++i)
+            acc = acc + or_bf16_to_f32(rows[i][h]);
+        out[h] = or_bf16_rne(acc);
+    }
+}
+
+/* Combine of one source token (s,t), given the layout: its rows are
+ * y[r][pos[s][t][r]] for r = 0..W-1 ascending with the slot in [0, cap);
+ * out_row = sum_rows of them and, if w_in is given, out_w_row[j] = the same
+ * ordered fp32 sum of w_in[r][p][j] (no rounding at the end).  y is uint16
+ * [W][cap][H], w_in float [W][cap][k]. */
 static void combine_token(int W, int k, int T, int H, int cap, int s, int t,
                           const int32_t *pos, const uint16_t *y,
                           const float *w_in, uint16_t *out_row, float *out_w_row)
 {
-    for (int h = 0; h < H; ++h) {
-        float acc = 0.0f;
-        for (int r = 0; r < W; ++r) {
-            int32_t p = pos[((int64_t)s * T + t) * W + r];
-            if (p < 0 || p >= cap) continue;
-            acc = acc + or_bf16_to_f32(y[((int64_t)r * cap + p) * H + h]);
-        }
-        out_row[h] = or_bf16_rne(acc);
+    const uint16_t *rows[64];
+    int nd = 0;
+    for (int r = 0; r < W; ++r) {
+        int32_t p = pos[((int64_t)s * T + t) * W + r];
+        if (p < 0 || p >= cap) continue;
+        rows[nd++] = y + ((int64_t)r * cap + p) * H;
     }
+    sum_rows(nd, rows, H, out_row);
     if (w_in && out_w_row) {
         for (int j = 0; j < k; ++j) {
             float acc = 0.0f;
@@ -391,6 +428,17 @@ static void combine_token(int W, int k, int T, int H, int cap, int s, int t,
             out_w_row[j] = acc;
         }
     }
+}
+
+/* Combine of one token whose nd rows (ascending rank order) are given
+ * gathered: rows [nd][H] -> out [H]. */
+int or_combine_gathered(int nd, int H, const uint16_t *rows, uint16_t *out)
+{
+    const uint16_t *ptrs[64];
+    if (nd < 0 || nd > 64) return OR_EINVAL;
+    for (int i = 0; i < nd; ++i) ptrs[i] = rows + (int64_t)i * H;
+    sum_rows(nd, ptrs, H, out);
+    return OR_OK;
 }
 
 /* Combine of every present token: out uint16 [W][T][H], out_w float

@@ -436,3 +436,35 @@ def test_combine_matches_bruteforce_wide_range(seed):
     got, _ = oracle.combine(wl, inp.num_tokens, res["pos"], y, None, res["cap"])
     for (s, t), row in out.items():
         assert np.array_equal(got[s, t], row)
+
+
+def test_sampled_row_functions_agree_with_whole_buffer_functions():
+    """The per-row forms used for full-size sampling give the same rows as
+    the whole-buffer forms pinned above."""
+    for name in ["dsv3", "dsv3_fp8_zipf"]:
+        wl = _reduced(name).scaled(40, hidden=256)
+        inp = gen.make_inputs(wl, num_tokens=gen.ragged_num_tokens(wl))
+        res = oracle.run_all(inp)
+        rng = np.random.default_rng(9)
+        rc = res["recv_count"]
+        ranks = np.array([r for r in range(wl.world_size) if rc[r] > 0])
+        rr = rng.choice(ranks, size=20)
+        pp = np.array([rng.integers(0, rc[r]) for r in rr])
+        d = oracle.dispatch_rows(wl, inp.x_bits, inp.weights, inp.indices,
+                                 inp.num_tokens, res["pos"], rr, pp)
+        assert np.array_equal(d["out"], res["out"][rr, pp])
+        assert np.array_equal(d["src_pos"], res["src_pos"][rr, pp])
+        if wl.fp8:
+            assert np.array_equal(d["out_scales"], res["out_scales"][rr, pp])
+        y = oracle.identity_rows(wl, rr, d["out"], d["out_scales"], d["out_w"],
+                                 d["out_idx"])
+        assert np.array_equal(y, res["y"][rr, pp])
+        T = wl.max_tokens_per_rank
+        for g in rng.choice(wl.world_size * T, size=10):
+            s, t = divmod(int(g), T)
+            if t >= inp.num_tokens[s]:
+                continue
+            rows = [res["y"][r, res["pos"][s, t, r]] for r in range(wl.world_size)
+                    if res["pos"][s, t, r] >= 0]
+            assert np.array_equal(oracle.combine_gathered(np.array(rows)),
+                                  res["combined"][s, t])
