@@ -15,6 +15,13 @@ _lock = threading.Lock()
 _lib = None
 
 EP_SUCCESS = 0
+EP_ERR_INVALID_ARGS = 3
+EP_ERR_NOT_FOUND = 4
+EP_ERR_BAD_STATE = 6
+EP_ERR_GPU_OP = 7
+EP_ERR_TIMEOUT = 8
+EP_ERR_CAPACITY = 9
+EP_ERR_BAD_INDEX = 10
 STATUS_NAMES = {
     0: "EP_SUCCESS", 1: "EP_INIT", 2: "EP_IN_PROGRESS",
     3: "EP_ERR_INVALID_ARGS", 4: "EP_ERR_NOT_FOUND", 5: "EP_ERR_RDMA_OP",

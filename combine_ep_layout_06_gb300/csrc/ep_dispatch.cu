@@ -138,7 +138,9 @@ dispatch_kernel(const DispatchParams p) {
 
         // payload
         const uint4 *src = p.x + tok * p.nvec;
-        for (int v0 = lane; v0 < p.nvec; v0 += 32 * U) {
+        // The trip count is warp-uniform (the FP8 path shuffles inside).
+        for (int base = 0; base < p.nvec; base += 32 * U) {
+            const int v0 = base + lane;
             if constexpr (!FP8) {
                 uint4 buf[U];
 #pragma unroll
