@@ -94,6 +94,7 @@ SIGNATURES = {
     "ep_reset": (_S, [_P, _P]),
     "ep_get_error": (_S, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
     "ep_test_identity_expert": (_S, [_P, _P, _I64, _P]),
+    "ep_layout_noalloc": (_S, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
 }
 
 

@@ -252,6 +252,32 @@ ep_status_t ep_get_error(ep_handle_t *h, uint32_t *mask, void *stream);
 ep_status_t ep_test_identity_expert(ep_handle_t *h, void *d_y,
                                     int64_t y_rank_stride_bytes, void *stream);
 
+/* Routing layout without any allocation, for callers that cannot allocate
+ * device memory or pass a workspace: code living inside another
+ * framework's memory pool that only sees raw tensor pointers, and serving
+ * paths that forbid cudaMalloc (it can synchronise the device and can fail
+ * under memory pressure).  The pages have no counterpart of this call; it
+ * computes the same layout as ep_layout + ep_dispatch (pos, send counts,
+ * recv_count) with no handle.
+ *   d_idx [W][T][k] int32, h_num_tokens [W] host; outputs (caller-owned,
+ *   device): d_pos [W][T][W] (-1 where r is not a destination),
+ *   d_send_counts [W][W], d_recv_count [W]; d_error: NULL or a device u32
+ *   that gets EP_DEVERR_BAD_INDEX OR-ed in (out-of-range ids contribute no
+ *   destination).
+ * Scratch is a fixed device array inside the library (about 1.06 MB, held
+ * by every GPU that loads the library until the process exits); it limits
+ * the layout to W <= 32 and W * ceil(T/32) <= 4128 chunks (131072 tokens
+ * for T a multiple of 32).  Larger sizes return EP_ERR_INVALID_ARGS.  The
+ * first call on a device looks the array up (with that device current);
+ * make it before any stream capture.  All calls share the array: calls
+ * whose work overlaps on the GPU race; order them on one stream. */
+ep_status_t ep_layout_noalloc(int32_t world_size, int32_t num_experts,
+                              int32_t topk, int32_t max_tokens_per_rank,
+                              const int32_t *d_idx, const int32_t *h_num_tokens,
+                              int32_t *d_pos, int32_t *d_send_counts,
+                              int32_t *d_recv_count, uint32_t *d_error,
+                              void *stream);
+
 #ifdef __cplusplus
 }
 #endif
