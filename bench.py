@@ -51,6 +51,10 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override T (tokens per rank), e.g. for a profiling case")
+    ap.add_argument("--cap", type=int, default=0,
+                    help="receive rows per rank (0: W*T)")
     return ap.parse_args()
 
 
@@ -187,6 +191,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     wl = gen.WORKLOADS[args.workload]
+    if args.tokens:
+        wl = wl.scaled(args.tokens)
     W, T, H, k = wl.world_size, wl.max_tokens_per_rank, wl.hidden, wl.topk
     inp = gen.make_inputs(wl)
     N = W * T
@@ -195,6 +201,7 @@ def run_ours(args, rank, world, local_rank):
                 for s in range(W) for t in range(T)))
 
     cfg = EpDispatchCombineConfig(W, wl.num_experts, k, H, T,
+                                  max_recv_tokens_per_rank=args.cap,
                                   dispatch_dtype="fp8_e4m3" if wl.fp8 else "bf16")
     op = EpDispatchCombineOp(cfg, device=dev)
     x = torch.from_numpy(inp.x_bits.view(np.int16)).to(dev).view(torch.bfloat16)

@@ -50,6 +50,7 @@ ep_status_t make_config(const ep_config_t *in, Config *c) {
     c->fp8 = fp8;
     c->nch = (T + kChunk - 1) / kChunk;
     c->G = W * c->nch;
+    c->Q = (c->G + kGroup - 1) / kGroup;
     c->nvec = H / 8;
     c->nb = fp8 ? H / EP_QUANT_BLOCK : 0;
     c->early_notify = env_flag("EP_EARLY_NOTIFY", in->early_notify ? 1 : 0) != 0;
@@ -91,8 +92,10 @@ void plan_workspace(const Config &c, char *base, Workspace *ws) {
     ws->words = reinterpret_cast<uint32_t *>(take(kCounterWords * 4));
     ws->dflags = reinterpret_cast<uint32_t *>(take(W * W * 4));
     ws->cflags = reinterpret_cast<uint32_t *>(take(W * W * 4));
-    ws->chunk_cnt = reinterpret_cast<int32_t *>(take(G * W * 4));
-    ws->chunk_base = reinterpret_cast<int32_t *>(take((G + 1) * W * 4));
+    const size_t Q = c.Q;
+    ws->chunk_local = reinterpret_cast<int32_t *>(take(G * W * 4));
+    ws->group_tot = reinterpret_cast<int32_t *>(take(Q * W * 4));
+    ws->group_base = reinterpret_cast<int32_t *>(take((Q + 1) * W * 4));
     ws->send_counts = reinterpret_cast<int32_t *>(take(W * W * 4));
     ws->recv_count = reinterpret_cast<int32_t *>(take(W * 4));
     ws->masks = reinterpret_cast<uint32_t *>(take(W * T * 4));
@@ -171,10 +174,10 @@ ep_status_t ep_create(const ep_config_t *cfg, void *d_workspace, size_t bytes,
     if (st == EP_SUCCESS)
         st = gpu(h, cudaEventCreateWithFlags(&h->ev_combine_sent, cudaEventDisableTiming),
                  "cudaEventCreate");
-    // zero the counters, flags and error word (everything before chunk_cnt)
+    // zero the counters, flags and error word (everything before chunk_local)
     if (st == EP_SUCCESS)
         st = gpu(h, cudaMemset(ws.words, 0,
-                               reinterpret_cast<char *>(ws.chunk_cnt) -
+                               reinterpret_cast<char *>(ws.chunk_local) -
                                    reinterpret_cast<char *>(ws.words)),
                  "cudaMemset");
     if (st == EP_SUCCESS) st = gpu(h, cudaDeviceSynchronize(), "cudaDeviceSynchronize");
@@ -454,7 +457,7 @@ ep_status_t ep_reset(ep_handle_t *h, void *stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const ep_status_t s = gpu(
         h, cudaMemsetAsync(h->ws.words, 0,
-                           reinterpret_cast<char *>(h->ws.chunk_cnt) -
+                           reinterpret_cast<char *>(h->ws.chunk_local) -
                                reinterpret_cast<char *>(h->ws.words),
                            st),
         "cudaMemsetAsync");

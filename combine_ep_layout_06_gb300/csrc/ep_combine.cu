@@ -24,7 +24,17 @@
 namespace ep {
 namespace {
 
-constexpr int kCombineWarps = 8;
+#ifndef EP_COMBINE_WARPS
+#define EP_COMBINE_WARPS 8
+#endif
+#ifndef EP_COMBINE_MIN_BLOCKS
+#define EP_COMBINE_MIN_BLOCKS 3    // 3 CTAs of 8 warps per SM: <= 80 registers
+#endif
+#ifndef EP_COMBINE_UNROLL8
+#define EP_COMBINE_UNROLL8 2       // column vectors in flight per row, <= 8 rows
+#endif
+
+constexpr int kCombineWarps = EP_COMBINE_WARPS;
 constexpr int kCombineThreads = kCombineWarps * 32;
 
 struct CombineParams {
@@ -89,7 +99,7 @@ __device__ void fused_receive_wait(const CombineParams &p) {
 }
 
 template <int MAXD, int U, bool COHERENT>
-__global__ void __launch_bounds__(kCombineThreads)
+__global__ void __launch_bounds__(kCombineThreads, EP_COMBINE_MIN_BLOCKS)
 combine_kernel(const CombineParams p) {
     if (p.fused_wait) fused_receive_wait(p);
 
@@ -286,7 +296,7 @@ cudaError_t launch_combine(const Config &c, const Workspace &ws,
     const int maxd = c.W < c.k ? c.W : c.k;   // |D(s,t)| <= min(W, k)
     if (maxd <= 2) return launch_combine_m<2, 4>(c, p, st);
     if (maxd <= 4) return launch_combine_m<4, 2>(c, p, st);
-    if (maxd <= 8) return launch_combine_m<8, 2>(c, p, st);
+    if (maxd <= 8) return launch_combine_m<8, EP_COMBINE_UNROLL8>(c, p, st);
     if (maxd <= 16) return launch_combine_m<16, 1>(c, p, st);
     return launch_combine_m<32, 1>(c, p, st);
 }
@@ -312,7 +322,7 @@ cudaError_t launch_identity_expert(const Config &c, const Workspace &ws,
     const int blocks = (int)((rows + 7) / 8);
     identity_expert_kernel<<<blocks, 256, 0, st>>>(
         ws.seg0, ws.seg_stride, ws.off_out, ws.off_scales, ws.off_w, ws.off_idx,
-        ws.chunk_base + (int64_t)c.G * c.W, y, y_stride, c.W, c.E, c.Er, c.k,
+        ws.group_base + (int64_t)c.Q * c.W, y, y_stride, c.W, c.E, c.Er, c.k,
         c.H, c.cap, c.fp8 ? 1 : 0);
     return cudaGetLastError();
 }

@@ -10,12 +10,17 @@
 // scale = fl32(a/448), q = RNE-satfinite(fl32(x/scale)), a == 0 -> scale 0,
 // codes 0.
 //
-// GB300 mapping.  One CTA per 32-token layout chunk.  Warp 0 turns the
-// chunk's masks and the chunk bases into receive slots (ballot + popc of the
-// lanes below) and writes pos; then each warp streams whole token rows: the
-// source row is read ONCE from HBM (16-byte non-allocating loads, U vectors
-// in flight per lane) and stored to each destination row with 16-byte
-// evict-first stores, 512 contiguous bytes per warp instruction.
+// GB300 mapping.  A CTA takes kTokensPerCta tokens of one 32-token layout
+// chunk.  Warp 0 turns the chunk's masks and base into receive slots
+// (ballot + popc of the lanes below) and writes pos.  Then either
+//  - the register path: each warp streams whole token rows, reading the
+//    source row ONCE from HBM (16-byte non-allocating loads, U vectors in
+//    flight per lane) and storing it to each destination row with 16-byte
+//    evict-first stores, 512 contiguous bytes per warp instruction (the FP8
+//    path quantises on the way: 16 elements per lane, 8 lanes per block);
+//  - the bulk path (bf16): one thread drives the Tensor Memory Accelerator
+//    with 1-D cp.async.bulk row copies through a ring of shared-memory
+//    stages, one load per source row and one bulk store per destination.
 #include <cuda_fp8.h>
 
 #include "ep_device.cuh"
@@ -23,16 +28,39 @@
 namespace ep {
 namespace {
 
-constexpr int kDispatchWarps = 4;
+#ifndef EP_DISPATCH_WARPS
+#define EP_DISPATCH_WARPS 4
+#endif
+#ifndef EP_DISPATCH_UNROLL
+#define EP_DISPATCH_UNROLL 4           // 16-byte vectors in flight per lane
+#endif
+#ifndef EP_DISPATCH_FP8_UNROLL
+#define EP_DISPATCH_FP8_UNROLL 2       // 32-byte element pairs per lane (FP8)
+#endif
+#ifndef EP_DISPATCH_BULK_STAGES
+#define EP_DISPATCH_BULK_STAGES 4      // 0: register path for bf16 rows too
+#endif
+#ifndef EP_DISPATCH_BULK_EVICT_FIRST
+#define EP_DISPATCH_BULK_EVICT_FIRST 1 // L2 evict-first hint on bulk copies
+#endif
+#ifndef EP_DISPATCH_TPC
+#define EP_DISPATCH_TPC 8              // tokens per CTA (divides the chunk)
+#endif
+
+constexpr int kDispatchWarps = EP_DISPATCH_WARPS;
 constexpr int kDispatchThreads = kDispatchWarps * 32;
+constexpr int kTokensPerCta = EP_DISPATCH_TPC;
+constexpr int kCtasPerChunk = kChunk / kTokensPerCta;
 constexpr int kMaxFp8Blocks = 128;   // H <= 16384 for FP8
+static_assert(kChunk % kTokensPerCta == 0, "tokens per CTA must divide the chunk");
 
 struct DispatchParams {
     const uint4 *x;
     const float *w;
     const int32_t *idx;
     const uint32_t *masks;
-    const int32_t *chunk_base;
+    const int32_t *chunk_local;
+    const int32_t *group_base;
     int32_t *pos;
     char *seg0;
     int64_t seg_stride, off_out, off_scales, off_w, off_idx, off_src;
@@ -41,6 +69,7 @@ struct DispatchParams {
     int W, k, T, H, nch, cap, nvec, nb;
     int notify;
     uint32_t epoch;
+    int64_t timeout_ns;
     TokenCounts nt;
 };
 
@@ -49,6 +78,81 @@ struct DispatchSmem {
     uint32_t mask[kChunk];
     float scales[kDispatchWarps][kMaxFp8Blocks];
 };
+
+struct BulkSmem {
+    int32_t pos[kChunk][EP_MAX_WORLD];
+    uint32_t mask[kChunk];
+    int32_t list[kChunk];
+};
+
+// Receive slots of the chunk's tokens (the within-chunk part of the layout):
+// warp 0 ballots each destination bit over the chunk's 32 tokens; a token's
+// slot on rank r is the chunk's start plus the number of lanes below it that
+// also go to r.  Fills spos / smask for all 32 tokens and writes pos for the
+// CTA's own tokens [i0, i0 + kTokensPerCta).
+__device__ __forceinline__ void chunk_slots(const DispatchParams &p, int g, int s,
+                                            int t0, int n_s, int i0,
+                                            int32_t (*spos)[EP_MAX_WORLD],
+                                            uint32_t *smask) {
+    const int lane = threadIdx.x & 31;
+    const int t = t0 + lane;
+    const uint32_t m = (t < n_s) ? p.masks[(int64_t)s * p.T + t] : 0u;
+    const int my_base = (lane < p.W) ? p.group_base[(int64_t)(g / kGroup) * p.W + lane] +
+                                           p.chunk_local[(int64_t)g * p.W + lane]
+                                     : 0;
+    const uint32_t below = lanemask_lt();
+    for (int r = 0; r < p.W; ++r) {
+        const uint32_t b = __ballot_sync(0xffffffffu, (m >> r) & 1u);
+        const int base = __shfl_sync(0xffffffffu, my_base, r);
+        spos[lane][r] = ((m >> r) & 1u) ? base + __popc(b & below) : -1;
+    }
+    smask[lane] = m;
+    if (t < p.T && lane >= i0 && lane < i0 + kTokensPerCta) {
+        int32_t *dst = p.pos + ((int64_t)s * p.T + t) * p.W;
+        for (int r = 0; r < p.W; ++r) dst[r] = spos[lane][r];
+    }
+}
+
+// Per-destination metadata of one token, written by one warp: all k
+// weights, all k expert ids, src_pos.
+__device__ __forceinline__ void token_metadata(const DispatchParams &p, int s, int t,
+                                               uint32_t m, const int32_t *slots) {
+    const int lane = threadIdx.x & 31;
+    const int64_t tok = (int64_t)s * p.T + t;
+    float wv = 0.f;
+    int32_t iv = 0;
+    if (lane < p.k) {
+        wv = __ldg(p.w + tok * p.k + lane);
+        iv = __ldg(p.idx + tok * p.k + lane);
+    }
+    for (uint32_t mm = m; mm; mm &= mm - 1u) {
+        const int r = __ffs(mm) - 1;
+        const int slot = slots[r];
+        if (slot >= p.cap) continue;
+        char *seg = p.seg0 + (int64_t)r * p.seg_stride;
+        if (lane < p.k) {
+            reinterpret_cast<float *>(seg + p.off_w)[(int64_t)slot * p.k + lane] = wv;
+            reinterpret_cast<int32_t *>(seg + p.off_idx)[(int64_t)slot * p.k + lane] = iv;
+        }
+        if (lane == 0)
+            reinterpret_cast<int32_t *>(seg + p.off_src)[slot] = (int32_t)(s * p.T + t);
+    }
+}
+
+// The last CTA of source s posts (s -> r) for every r, zero-count pairs
+// included, after all of s's rows are stored.
+__device__ __forceinline__ void notify_source_done(const DispatchParams &p, int s) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t tk = atom_add_acq_rel_gpu(p.words + kWordSrcDone + s, 1u);
+        if (tk == (uint32_t)(p.nch * kCtasPerChunk) - 1u) {
+            p.words[kWordSrcDone + s] = 0u;
+            for (int r = 0; r < p.W; ++r)
+                st_release_gpu(p.dflags + r * p.W + s, p.epoch);
+        }
+    }
+}
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float f[8]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -59,24 +163,21 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float f[8]) {
     }
 }
 
-// 8 values -> 8 E4M3 codes (byte i = element i) given the block scale.
-__device__ __forceinline__ uint2 quant8(const float f[8], float scale) {
-    uint32_t word[2];
+// 4 values -> 4 E4M3 codes (byte i = element i) given the block scale.
+__device__ __forceinline__ uint32_t quant4(const float *f, float scale) {
+    uint32_t packed = 0;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint32_t packed = 0;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const float a = f[4 * h + 2 * i] / scale;
-            const float b = f[4 * h + 2 * i + 1] / scale;
-            const __nv_fp8x2_storage_t q =
-                __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-            packed |= (uint32_t)q << (16 * i);
-        }
-        word[h] = packed;
+    for (int i = 0; i < 2; ++i) {
+        const float a = f[2 * i] / scale;
+        const float b = f[2 * i + 1] / scale;
+        const __nv_fp8x2_storage_t q =
+            __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+        packed |= (uint32_t)q << (16 * i);
     }
-    return make_uint2(word[0], word[1]);
+    return packed;
 }
+
+// ------------------------------------------------------------ register path
 
 template <bool FP8, int U>
 __global__ void __launch_bounds__(kDispatchThreads)
@@ -84,64 +185,28 @@ dispatch_kernel(const DispatchParams p) {
     __shared__ DispatchSmem sm;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int g = blockIdx.x;
+    const int g = blockIdx.x / kCtasPerChunk;
+    const int i0 = (blockIdx.x - g * kCtasPerChunk) * kTokensPerCta;
     const int s = g / p.nch;
     const int t0 = (g - s * p.nch) * kChunk;
     const int n_s = p.nt.n[s];
 
-    // ---- receive slots of the chunk's tokens (layout, within-chunk part)
-    if (warp == 0) {
-        const int t = t0 + lane;
-        const uint32_t m = (t < n_s) ? p.masks[(int64_t)s * p.T + t] : 0u;
-        const int my_base = (lane < p.W) ? p.chunk_base[(int64_t)g * p.W + lane] : 0;
-        const uint32_t below = lanemask_lt();
-        for (int r = 0; r < p.W; ++r) {
-            const uint32_t b = __ballot_sync(0xffffffffu, (m >> r) & 1u);
-            const int base = __shfl_sync(0xffffffffu, my_base, r);
-            sm.pos[lane][r] = ((m >> r) & 1u) ? base + __popc(b & below) : -1;
-        }
-        sm.mask[lane] = m;
-        if (t < p.T) {
-            int32_t *dst = p.pos + ((int64_t)s * p.T + t) * p.W;
-            for (int r = 0; r < p.W; ++r) dst[r] = sm.pos[lane][r];
-        }
-    }
+    if (warp == 0) chunk_slots(p, g, s, t0, n_s, i0, sm.pos, sm.mask);
     __syncthreads();
 
-    // ---- rows
-    for (int i = warp; i < kChunk; i += kDispatchWarps) {
+    for (int i = i0 + warp; i < i0 + kTokensPerCta; i += kDispatchWarps) {
         const int t = t0 + i;
         if (t >= n_s) break;
         const uint32_t m = sm.mask[i];
         if (m == 0u) continue;
         const int64_t tok = (int64_t)s * p.T + t;
+        token_metadata(p, s, t, m, sm.pos[i]);
 
-        // metadata: all k weights, all k ids, src_pos
-        float wv = 0.f;
-        int32_t iv = 0;
-        if (lane < p.k) {
-            wv = __ldg(p.w + tok * p.k + lane);
-            iv = __ldg(p.idx + tok * p.k + lane);
-        }
-        for (uint32_t mm = m; mm; mm &= mm - 1u) {
-            const int r = __ffs(mm) - 1;
-            const int slot = sm.pos[i][r];
-            if (slot >= p.cap) continue;
-            char *seg = p.seg0 + (int64_t)r * p.seg_stride;
-            if (lane < p.k) {
-                reinterpret_cast<float *>(seg + p.off_w)[(int64_t)slot * p.k + lane] = wv;
-                reinterpret_cast<int32_t *>(seg + p.off_idx)[(int64_t)slot * p.k + lane] = iv;
-            }
-            if (lane == 0)
-                reinterpret_cast<int32_t *>(seg + p.off_src)[slot] = (int32_t)(s * p.T + t);
-        }
-
-        // payload
         const uint4 *src = p.x + tok * p.nvec;
-        // The trip count is warp-uniform (the FP8 path shuffles inside).
-        for (int base = 0; base < p.nvec; base += 32 * U) {
-            const int v0 = base + lane;
-            if constexpr (!FP8) {
+        if constexpr (!FP8) {
+            // The trip count is warp-uniform.
+            for (int base = 0; base < p.nvec; base += 32 * U) {
+                const int v0 = base + lane;
                 uint4 buf[U];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
@@ -161,45 +226,58 @@ dispatch_kernel(const DispatchParams p) {
                         if (v < p.nvec) st_stream16(dst + v, buf[u]);
                     }
                 }
-            } else {
-                uint2 q[U];
+            }
+        } else {
+            // A lane takes a pair of 16-byte vectors (16 elements); 8 lanes
+            // hold one 128-element block; the warp covers 4 blocks per pair
+            // index step.  npair = H/16 is a multiple of 8, so groups of 8
+            // lanes are either wholly in range or wholly out of it, and the
+            // trip count is warp-uniform (the amax shuffles need all lanes).
+            const int npair = p.nvec >> 1;
+            for (int base = 0; base < npair; base += 32 * U) {
+                uint4 q[U];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    const int v = v0 + 32 * u;
-                    const bool active = v < p.nvec;   // whole half-warps
-                    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-                    if (active) raw = ld_stream16(src + v);
-                    float f[8];
-                    unpack_bf16x8(raw, f);
+                    const int pv = base + lane + 32 * u;
+                    const bool active = pv < npair;
+                    uint4 r0 = make_uint4(0u, 0u, 0u, 0u), r1 = r0;
+                    if (active) {
+                        r0 = ld_stream16(src + 2 * pv);
+                        r1 = ld_stream16(src + 2 * pv + 1);
+                    }
+                    float f[16];
+                    unpack_bf16x8(r0, f);
+                    unpack_bf16x8(r1, f + 8);
                     float a = 0.f;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(f[e]));
+                    for (int e = 0; e < 16; ++e) a = fmaxf(a, fabsf(f[e]));
 #pragma unroll
-                    for (int o = 8; o > 0; o >>= 1)
+                    for (int o = 4; o > 0; o >>= 1)
                         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
                     float scale = 0.f;
-                    q[u] = make_uint2(0u, 0u);
+                    q[u] = make_uint4(0u, 0u, 0u, 0u);
                     if (a != 0.f) {
                         scale = a / 448.0f;
-                        q[u] = quant8(f, scale);
+                        q[u].x = quant4(f, scale);
+                        q[u].y = quant4(f + 4, scale);
+                        q[u].z = quant4(f + 8, scale);
+                        q[u].w = quant4(f + 12, scale);
                     }
-                    if (active && (lane & 15) == 0) sm.scales[warp][v >> 4] = scale;
+                    if (active && (lane & 7) == 0) sm.scales[warp][pv >> 3] = scale;
                 }
                 for (uint32_t mm = m; mm; mm &= mm - 1u) {
                     const int r = __ffs(mm) - 1;
                     const int slot = sm.pos[i][r];
                     if (slot >= p.cap) continue;
-                    char *dst = p.seg0 + (int64_t)r * p.seg_stride + p.off_out +
-                                (int64_t)slot * p.H;
+                    uint4 *dst = reinterpret_cast<uint4 *>(
+                        p.seg0 + (int64_t)r * p.seg_stride + p.off_out + (int64_t)slot * p.H);
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
-                        const int v = v0 + 32 * u;
-                        if (v < p.nvec) st_stream8(dst + (int64_t)v * 8, q[u]);
+                        const int pv = base + lane + 32 * u;
+                        if (pv < npair) st_stream16(dst + pv, q[u]);
                     }
                 }
             }
-        }
-        if constexpr (FP8) {
             __syncwarp();
             for (uint32_t mm = m; mm; mm &= mm - 1u) {
                 const int r = __ffs(mm) - 1;
@@ -214,20 +292,182 @@ dispatch_kernel(const DispatchParams p) {
         }
     }
 
-    // ---- ready notification: the last CTA of source s posts (s -> r) for
-    // every r, zero-count pairs included, after all of s's rows are stored.
-    if (p.notify) {
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const uint32_t tk = atom_add_acq_rel_gpu(p.words + kWordSrcDone + s, 1u);
-            if (tk == (uint32_t)p.nch - 1u) {
-                p.words[kWordSrcDone + s] = 0u;
-                for (int r = 0; r < p.W; ++r)
-                    st_release_gpu(p.dflags + r * p.W + s, p.epoch);
-            }
+    if (p.notify) notify_source_done(p, s);
+}
+
+// ---------------------------------------------------------------- bulk path
+// bf16 rows by the Tensor Memory Accelerator's bulk copies: thread 0 runs a
+// ring of STAGES row buffers in shared memory.  Each source row is brought
+// in ONCE by cp.async.bulk (completion counted on an mbarrier), then one
+// bulk store per destination writes it out; a stage is refilled once the
+// bulk stores that read it have finished reading.  Warps 1.. write the
+// per-row metadata meanwhile.  Every mbarrier wait is bounded.
+
+__device__ __forceinline__ uint32_t smem_u32(const void *ptr) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+// Bounded: gives up after timeout_ns of %globaltimer or 2^26 polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          int64_t timeout_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0; it < (1u << 26); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((int64_t)(globaltimer_ns() - t0) > timeout_ns) return false;
+    }
+    return false;
+}
+// L2 policy for data touched once: evict first.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes,
+                                          uint64_t *bar, uint64_t pol) {
+#if EP_DISPATCH_BULK_EVICT_FIRST
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+                 "[%0], [%1], %2, [%3], %4;"
+                 :: "r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+                 : "memory");
+#else
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+                 "[%0], [%1], %2, [%3];"
+                 :: "r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+#endif
+}
+__device__ __forceinline__ void bulk_store(void *gdst, const void *smem_src, uint32_t bytes,
+                                           uint64_t pol) {
+#if EP_DISPATCH_BULK_EVICT_FIRST
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
+                 :: "l"(gdst), "r"(smem_u32(smem_src)), "r"(bytes), "l"(pol) : "memory");
+#else
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(gdst), "r"(smem_u32(smem_src)), "r"(bytes) : "memory");
+#endif
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+template <int STAGES>
+__global__ void __launch_bounds__(kDispatchThreads)
+dispatch_bulk_kernel(const DispatchParams p) {
+    extern __shared__ __align__(128) unsigned char stage_buf[];
+    __shared__ BulkSmem sm;
+    __shared__ __align__(8) uint64_t bar[STAGES];
+    __shared__ int s_n;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int g = blockIdx.x / kCtasPerChunk;
+    const int i0 = (blockIdx.x - g * kCtasPerChunk) * kTokensPerCta;
+    const int s = g / p.nch;
+    const int t0 = (g - s * p.nch) * kChunk;
+    const int n_s = p.nt.n[s];
+
+    if (warp == 0) {
+        chunk_slots(p, g, s, t0, n_s, i0, sm.pos, sm.mask);
+        __syncwarp();
+        if (lane == 0) {
+            int n = 0;
+            for (int i = i0; i < i0 + kTokensPerCta; ++i)
+                if (t0 + i < n_s && sm.mask[i]) sm.list[n++] = i;
+            s_n = n;
+            for (int i = 0; i < STAGES; ++i) mbar_init(&bar[i], 1);
+            mbar_init_fence();
         }
     }
+    __syncthreads();
+    const int n = s_n;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint32_t bytes = (uint32_t)p.nvec * 16u;
+            const uint64_t pol = l2_evict_first_policy();
+            auto issue = [&](int j) {
+                const int st = j % STAGES;
+                const char *src = reinterpret_cast<const char *>(p.x) +
+                                  ((int64_t)s * p.T + t0 + sm.list[j]) * bytes;
+                mbar_expect_tx(&bar[st], bytes);
+                bulk_load(stage_buf + (size_t)st * bytes, src, bytes, &bar[st], pol);
+            };
+            const int pre = n < STAGES ? n : STAGES;
+            for (int j = 0; j < pre; ++j) issue(j);
+            int issued = pre;
+            bool ok = true;
+            for (int j = 0; j < n; ++j) {
+                const int st = j % STAGES;
+                if (!mbar_wait(&bar[st], (uint32_t)(j / STAGES) & 1u, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                const int i = sm.list[j];
+                const uint32_t m = sm.mask[i];
+                const unsigned char *src = stage_buf + (size_t)st * bytes;
+                for (uint32_t mm = m; mm; mm &= mm - 1u) {
+                    const int r = __ffs(mm) - 1;
+                    const int slot = sm.pos[i][r];
+                    if (slot >= p.cap) continue;
+                    bulk_store(p.seg0 + (int64_t)r * p.seg_stride + p.off_out +
+                                   (int64_t)slot * bytes,
+                               src, bytes, pol);
+                }
+                bulk_commit();
+                // refill the stage of token j-1: its stores were committed one
+                // group ago, so waiting until at most the newest group is still
+                // reading frees it
+                if (j >= 1 && issued < n) {
+                    bulk_wait_read1();
+                    issue(issued);
+                    ++issued;
+                }
+            }
+            if (!ok) {
+                set_error(p.words, EP_DEVERR_TIMEOUT);
+                // drain the loads still in flight (bounded), so no copy
+                // writes shared memory after the CTA has gone
+                for (int j = 0; j < issued; ++j)
+                    mbar_wait(&bar[j % STAGES], (uint32_t)(j / STAGES) & 1u, p.timeout_ns);
+            }
+            bulk_wait_all();
+            // order the bulk (async-proxy) row writes before the generic
+            // release of the ready flags
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        __syncwarp();
+    } else {
+        for (int j = warp - 1; j < n; j += kDispatchWarps - 1) {
+            const int i = sm.list[j];
+            token_metadata(p, s, t0 + i, sm.mask[i], sm.pos[i]);
+        }
+    }
+
+    if (p.notify) notify_source_done(p, s);
 }
 
 __global__ void dispatch_recv_kernel(uint32_t *dflags, uint32_t *words,
@@ -246,7 +486,23 @@ __global__ void dispatch_recv_kernel(uint32_t *dflags, uint32_t *words,
 template <bool FP8, int U>
 cudaError_t launch_dispatch_t(const Config &c, const DispatchParams &p,
                               cudaStream_t st) {
-    dispatch_kernel<FP8, U><<<c.G, kDispatchThreads, 0, st>>>(p);
+    dispatch_kernel<FP8, U><<<c.G * kCtasPerChunk, kDispatchThreads, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <int STAGES>
+cudaError_t launch_dispatch_bulk(const Config &c, const DispatchParams &p,
+                                 cudaStream_t st) {
+    const size_t dyn = (size_t)STAGES * c.nvec * 16;
+    static size_t configured = 48 * 1024;     // per instantiation
+    if (dyn > configured) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            dispatch_bulk_kernel<STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            (int)dyn);
+        if (e != cudaSuccess) return e;
+        configured = dyn;
+    }
+    dispatch_bulk_kernel<STAGES><<<c.G * kCtasPerChunk, kDispatchThreads, dyn, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -259,7 +515,8 @@ cudaError_t launch_dispatch(const Config &c, const Workspace &ws,
     p.w = a.w;
     p.idx = a.idx;
     p.masks = ws.masks;
-    p.chunk_base = ws.chunk_base;
+    p.chunk_local = ws.chunk_local;
+    p.group_base = ws.group_base;
     p.pos = ws.pos;
     p.seg0 = ws.seg0;
     p.seg_stride = ws.seg_stride;
@@ -274,9 +531,14 @@ cudaError_t launch_dispatch(const Config &c, const Workspace &ws,
     p.nvec = c.nvec; p.nb = c.nb;
     p.notify = c.early_notify ? 1 : 0;
     p.epoch = a.epoch;
+    p.timeout_ns = c.timeout_ns;
     p.nt = a.nt;
-    if (c.fp8) return launch_dispatch_t<true, 4>(c, p, st);
-    return launch_dispatch_t<false, 4>(c, p, st);
+    if (c.fp8) return launch_dispatch_t<true, EP_DISPATCH_FP8_UNROLL>(c, p, st);
+#if EP_DISPATCH_BULK_STAGES > 0
+    if ((size_t)EP_DISPATCH_BULK_STAGES * c.nvec * 16 <= 160 * 1024)
+        return launch_dispatch_bulk<EP_DISPATCH_BULK_STAGES>(c, p, st);
+#endif
+    return launch_dispatch_t<false, EP_DISPATCH_UNROLL>(c, p, st);
 }
 
 cudaError_t launch_dispatch_recv(const Config &c, const Workspace &ws,
@@ -284,7 +546,7 @@ cudaError_t launch_dispatch_recv(const Config &c, const Workspace &ws,
                                  cudaStream_t st) {
     const int threads = ((c.W * c.W + 31) / 32) * 32;
     dispatch_recv_kernel<<<1, threads, 0, st>>>(
-        ws.dflags, ws.words, ws.chunk_base + (int64_t)c.G * c.W, ws.recv_count,
+        ws.dflags, ws.words, ws.group_base + (int64_t)c.Q * c.W, ws.recv_count,
         c.W, check_flags ? 1 : 0, epoch, c.timeout_ns);
     return cudaGetLastError();
 }

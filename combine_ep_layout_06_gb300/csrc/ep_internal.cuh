@@ -12,6 +12,9 @@ namespace ep {
 // Tokens per layout chunk: one warp ballots over 32 tokens, so a chunk's
 // per-destination counts come from one __ballot_sync + __popc each.
 constexpr int kChunk = 32;
+// Chunks per layout group (one layout CTA of 8 warps): the group prefix is
+// computed inside the CTA, so the one global scan runs over groups only.
+constexpr int kGroup = 8;
 
 // Offsets of the small counters at the start of the workspace (u32 words).
 constexpr int kWordErr = 0;        // sticky device error word
@@ -24,8 +27,9 @@ struct Workspace {
     uint32_t *words;       // kCounterWords u32
     uint32_t *dflags;      // [W dst][W src]
     uint32_t *cflags;      // [W src][W dst]
-    int32_t *chunk_cnt;    // [G][W]   per-chunk destination counts
-    int32_t *chunk_base;   // [G+1][W] exclusive prefix over chunks; row G = totals
+    int32_t *chunk_local;  // [G][W]   exclusive prefix of a chunk within its group
+    int32_t *group_tot;    // [Q][W]   destination counts of each group
+    int32_t *group_base;   // [Q+1][W] exclusive prefix over groups; row Q = totals
     int32_t *send_counts;  // [W][W]
     int32_t *recv_count;   // [W] published by the receive step
     uint32_t *masks;       // [W][T]   destination-rank bit mask per token
@@ -42,6 +46,7 @@ struct Config {
     bool fp8;
     int nch;     // chunks per source rank = ceil(T / kChunk)
     int G;       // W * nch
+    int Q;       // layout groups = ceil(G / kGroup)
     int nvec;    // 16-byte vectors per bf16 row = H / 8
     int nb;      // FP8 blocks per row = H / 128 (0 for bf16)
     bool early_notify, fused_recv;

@@ -1,49 +1,64 @@
 // Routing layout (the step behind dispatch's recv_count and the receive
 // order): per-token destination-rank masks, per-chunk destination counts by
-// warp ballot, and -- in the last CTA to finish -- the exclusive prefix over
-// chunks in (source rank, chunk) order that fixes every receive position.
+// warp ballot, the prefix of each chunk inside its CTA's group of 8 chunks,
+// and -- in the last CTA to finish -- the exclusive prefix over groups in
+// (source rank, chunk) order that fixes every receive position.
 //
 // Definition (ROCm MORI "Communication APIs", MORI-EP, "EpDispatchCombineOp
 // methods": dispatch routes each token to its expert ranks and returns
 // recv_count): D(s,t) = { idx[s][t][j] / Er }, C[s][r] = #{t < n_s : r in
 // D(s,t)}, recv_count[r] = sum_s C[s][r]; rows on rank r are ordered by
-// (source rank, source token).  The chunk bases computed here plus the
-// within-chunk ballot prefix (recomputed by the dispatch kernel) give
-// pos[s][t][r] = sum_{s'<s} C[s'][r] + #{t' < t : r in D(s,t')}.
+// (source rank, source token).  Group base + chunk-in-group prefix computed
+// here plus the within-chunk ballot prefix (recomputed by the dispatch
+// kernel) give pos[s][t][r] = sum_{s'<s} C[s'][r] + #{t' < t : r in D(s,t')}.
 #include "ep_device.cuh"
 
 namespace ep {
 namespace {
 
-constexpr int kLayoutThreads = 256;            // 8 warps = 8 chunks per CTA
-constexpr int kLayoutWarps = kLayoutThreads / 32;
+constexpr int kLayoutThreads = kGroup * 32;     // one warp per chunk
+constexpr int kLayoutWarps = kGroup;
+constexpr int kScanBatch = 8;                   // group totals in registers per lane
 
 struct LayoutParams {
     const int32_t *idx;
     uint32_t *masks;
-    int32_t *chunk_cnt;
-    int32_t *chunk_base;
+    int32_t *chunk_local;
+    int32_t *group_tot;
+    int32_t *group_base;
     int32_t *send_counts;
     int32_t *recv_count;
     uint32_t *words;
-    int W, E, Er, k, T, nch, G, cap;
+    int W, E, Er, k, T, nch, G, Q, cap;
     int publish;             // also write recv_count (one-stream dispatch)
     TokenCounts nt;
 };
 
+// Start of chunk g in its destinations' receive order, once group_base is
+// final (g == G gives the totals).
+__device__ __forceinline__ int chunk_start(const LayoutParams &p, int g, int r) {
+    if (g >= p.G) return __ldcg(p.group_base + (int64_t)p.Q * p.W + r);
+    return __ldcg(p.group_base + (int64_t)(g / kGroup) * p.W + r) +
+           __ldcg(p.chunk_local + (int64_t)g * p.W + r);
+}
+
 __global__ void __launch_bounds__(kLayoutThreads)
 layout_kernel(const LayoutParams p) {
+    __shared__ int s_cnt[kLayoutWarps][EP_MAX_WORLD];
+    __shared__ int s_last;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int g = blockIdx.x * kLayoutWarps + warp;
+    const int q = blockIdx.x;
+    const int g = q * kGroup + warp;
 
+    // ---- per chunk: masks and destination counts (warp ballot)
+    int my_count = 0;
     if (g < p.G) {
         const int s = g / p.nch;
         const int t = (g - s * p.nch) * kChunk + lane;
-        const bool present = t < p.nt.n[s];
         uint32_t mask = 0;
         bool bad = false;
-        if (present) {
+        if (t < p.nt.n[s]) {
             const int32_t *row = p.idx + ((int64_t)s * p.T + t) * p.k;
             for (int j = 0; j < p.k; ++j) {
                 const int32_t e = __ldg(row + j);
@@ -55,58 +70,78 @@ layout_kernel(const LayoutParams p) {
         }
         if (bad) set_error(p.words, EP_DEVERR_BAD_INDEX);
         if (t < p.T) p.masks[(int64_t)s * p.T + t] = mask;
-        int my_count = 0;
         for (int r = 0; r < p.W; ++r) {
             const uint32_t b = __ballot_sync(0xffffffffu, (mask >> r) & 1u);
             if (lane == r) my_count = __popc(b);
         }
-        if (lane < p.W) p.chunk_cnt[(int64_t)g * p.W + lane] = my_count;
+    }
+    s_cnt[warp][lane] = my_count;
+    __syncthreads();
+
+    // ---- per group: prefix of each chunk inside the group, group totals
+    if (warp == 0 && lane < p.W) {
+        int run = 0;
+        for (int w = 0; w < kLayoutWarps; ++w) {
+            const int gg = q * kGroup + w;
+            if (gg < p.G) p.chunk_local[(int64_t)gg * p.W + lane] = run;
+            run += s_cnt[w][lane];
+        }
+        p.group_tot[(int64_t)q * p.W + lane] = run;
     }
 
-    // Last CTA to arrive turns the chunk counts into chunk bases.
-    __shared__ int s_last;
+    // ---- the last CTA to arrive scans the group totals
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0)
-        s_last = atom_add_acq_rel_gpu(p.words + kWordLayoutDone, 1u) ==
-                 gridDim.x - 1;
+        s_last = atom_add_acq_rel_gpu(p.words + kWordLayoutDone, 1u) == gridDim.x - 1;
     __syncthreads();
     if (!s_last) return;
     __threadfence();
 
-    // Warp `warp` scans destinations r = warp, warp + 8, ...  Each lane owns
-    // a contiguous run of chunks; a warp shuffle scan joins the runs.
-    const int per = (p.G + 31) / 32;
-    const int g0 = min(p.G, lane * per);
-    const int g1 = min(p.G, g0 + per);
+    // Warp w scans destinations r = w, w + 8, ...; each lane owns a
+    // contiguous run of groups, loaded kScanBatch at a time into registers.
+    const int per = (p.Q + 31) / 32;
+    const int q0 = min(p.Q, lane * per);
+    const int q1 = min(p.Q, q0 + per);
     for (int r = warp; r < p.W; r += kLayoutWarps) {
         int sum = 0;
-        for (int gg = g0; gg < g1; ++gg)
-            sum += __ldcg(p.chunk_cnt + (int64_t)gg * p.W + r);
+        for (int b0 = q0; b0 < q1; b0 += kScanBatch) {
+            int v[kScanBatch];
+#pragma unroll
+            for (int i = 0; i < kScanBatch; ++i)
+                v[i] = (b0 + i < q1) ? __ldcg(p.group_tot + (int64_t)(b0 + i) * p.W + r) : 0;
+#pragma unroll
+            for (int i = 0; i < kScanBatch; ++i) sum += v[i];
+        }
         int incl = sum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
+            const int x = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += x;
         }
         int run = incl - sum;
-        for (int gg = g0; gg < g1; ++gg) {
-            p.chunk_base[(int64_t)gg * p.W + r] = run;
-            run += __ldcg(p.chunk_cnt + (int64_t)gg * p.W + r);
+        for (int b0 = q0; b0 < q1; b0 += kScanBatch) {
+            int v[kScanBatch];
+#pragma unroll
+            for (int i = 0; i < kScanBatch; ++i)
+                v[i] = (b0 + i < q1) ? __ldcg(p.group_tot + (int64_t)(b0 + i) * p.W + r) : 0;
+#pragma unroll
+            for (int i = 0; i < kScanBatch; ++i) {
+                if (b0 + i < q1) p.group_base[(int64_t)(b0 + i) * p.W + r] = run;
+                run += v[i];
+            }
         }
-        const int total = __shfl_sync(0xffffffffu, incl, 31);
-        if (lane == 0) {
-            p.chunk_base[(int64_t)p.G * p.W + r] = total;
-            if (total > p.cap) set_error(p.words, EP_DEVERR_CAPACITY);
-            if (p.publish) p.recv_count[r] = total;
+        if (lane == 31) {
+            p.group_base[(int64_t)p.Q * p.W + r] = incl;
+            if (incl > p.cap) set_error(p.words, EP_DEVERR_CAPACITY);
+            if (p.publish) p.recv_count[r] = incl;
         }
-        __syncwarp();
-        // C[s][r] = base of the first chunk of s+1 minus that of s.
-        for (int s = lane; s < p.W; s += 32) {
-            const int b0 = __ldcg(p.chunk_base + (int64_t)s * p.nch * p.W + r);
-            const int b1 = __ldcg(p.chunk_base + (int64_t)(s + 1) * p.nch * p.W + r);
-            p.send_counts[s * p.W + r] = b1 - b0;
-        }
+    }
+    __syncthreads();
+    // C[s][r] = start of the first chunk of s+1 minus that of s.
+    for (int i = threadIdx.x; i < p.W * p.W; i += kLayoutThreads) {
+        const int s = i / p.W, r = i - s * p.W;
+        p.send_counts[i] = chunk_start(p, (s + 1) * p.nch, r) - chunk_start(p, s * p.nch, r);
     }
     if (threadIdx.x == 0) p.words[kWordLayoutDone] = 0;   // for the next call
 }
@@ -119,17 +154,17 @@ cudaError_t launch_layout(const Config &c, const Workspace &ws,
     LayoutParams p;
     p.idx = idx;
     p.masks = ws.masks;
-    p.chunk_cnt = ws.chunk_cnt;
-    p.chunk_base = ws.chunk_base;
+    p.chunk_local = ws.chunk_local;
+    p.group_tot = ws.group_tot;
+    p.group_base = ws.group_base;
     p.send_counts = ws.send_counts;
     p.recv_count = ws.recv_count;
     p.words = ws.words;
     p.W = c.W; p.E = c.E; p.Er = c.Er; p.k = c.k; p.T = c.T;
-    p.nch = c.nch; p.G = c.G; p.cap = c.cap;
+    p.nch = c.nch; p.G = c.G; p.Q = c.Q; p.cap = c.cap;
     p.publish = publish ? 1 : 0;
     p.nt = nt;
-    const int blocks = (c.G + kLayoutWarps - 1) / kLayoutWarps;
-    layout_kernel<<<blocks, kLayoutThreads, 0, st>>>(p);
+    layout_kernel<<<c.Q, kLayoutThreads, 0, st>>>(p);
     return cudaGetLastError();
 }
 
