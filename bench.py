@@ -289,7 +289,8 @@ def run_ours(args, rank, world, local_rank):
     dominant = "combine" if c_ms >= d_ms else "dispatch"
     dom_ms = c_ms if dominant == "combine" else d_ms
     achieved = ab[dominant] / (dom_ms / 1e3) / 1e9
-    kname = "combine_kernel" if dominant == "combine" else "dispatch_kernel"
+    kname = ("combine_kernel" if dominant == "combine"
+             else ("dispatch_kernel" if wl.fp8 else "dispatch_bulk_kernel"))
 
     # end to end: pinned host inputs -> device, path, combined output -> host
     e2e = None

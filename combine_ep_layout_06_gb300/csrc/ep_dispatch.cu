@@ -10,7 +10,7 @@
 // scale = fl32(a/448), q = RNE-satfinite(fl32(x/scale)), a == 0 -> scale 0,
 // codes 0.
 //
-// GB300 mapping.  A CTA takes kTokensPerCta tokens of one 32-token layout
+// GB300 mapping.  A CTA takes a few tokens (TPC) of one 32-token layout
 // chunk.  Warp 0 turns the chunk's masks and base into receive slots
 // (ballot + popc of the lanes below) and writes pos.  Then either
 //  - the register path: each warp streams whole token rows, reading the
@@ -35,24 +35,29 @@ namespace {
 #define EP_DISPATCH_UNROLL 4           // 16-byte vectors in flight per lane
 #endif
 #ifndef EP_DISPATCH_FP8_UNROLL
-#define EP_DISPATCH_FP8_UNROLL 2       // 32-byte element pairs per lane (FP8)
+#define EP_DISPATCH_FP8_UNROLL 1       // 32-byte element pairs per lane (FP8)
 #endif
 #ifndef EP_DISPATCH_BULK_STAGES
 #define EP_DISPATCH_BULK_STAGES 4      // 0: register path for bf16 rows too
+#endif
+#ifndef EP_DISPATCH_BULK_CTAS_PER_SM
+#define EP_DISPATCH_BULK_CTAS_PER_SM 2 // resident bulk CTAs per SM (0: no cap)
 #endif
 #ifndef EP_DISPATCH_BULK_EVICT_FIRST
 #define EP_DISPATCH_BULK_EVICT_FIRST 1 // L2 evict-first hint on bulk copies
 #endif
 #ifndef EP_DISPATCH_TPC
-#define EP_DISPATCH_TPC 8              // tokens per CTA (divides the chunk)
+#define EP_DISPATCH_TPC 2              // tokens per CTA, bulk path (divides 32)
+#endif
+#ifndef EP_DISPATCH_REG_TPC
+#define EP_DISPATCH_REG_TPC 4          // tokens per CTA, register / FP8 path
 #endif
 
 constexpr int kDispatchWarps = EP_DISPATCH_WARPS;
 constexpr int kDispatchThreads = kDispatchWarps * 32;
-constexpr int kTokensPerCta = EP_DISPATCH_TPC;
-constexpr int kCtasPerChunk = kChunk / kTokensPerCta;
 constexpr int kMaxFp8Blocks = 128;   // H <= 16384 for FP8
-static_assert(kChunk % kTokensPerCta == 0, "tokens per CTA must divide the chunk");
+static_assert(kChunk % EP_DISPATCH_TPC == 0 && kChunk % EP_DISPATCH_REG_TPC == 0,
+              "tokens per CTA must divide the chunk");
 
 struct DispatchParams {
     const uint4 *x;
@@ -89,7 +94,8 @@ struct BulkSmem {
 // warp 0 ballots each destination bit over the chunk's 32 tokens; a token's
 // slot on rank r is the chunk's start plus the number of lanes below it that
 // also go to r.  Fills spos / smask for all 32 tokens and writes pos for the
-// CTA's own tokens [i0, i0 + kTokensPerCta).
+// CTA's own tokens [i0, i0 + TPC).
+template <int TPC>
 __device__ __forceinline__ void chunk_slots(const DispatchParams &p, int g, int s,
                                             int t0, int n_s, int i0,
                                             int32_t (*spos)[EP_MAX_WORLD],
@@ -107,7 +113,7 @@ __device__ __forceinline__ void chunk_slots(const DispatchParams &p, int g, int 
         spos[lane][r] = ((m >> r) & 1u) ? base + __popc(b & below) : -1;
     }
     smask[lane] = m;
-    if (t < p.T && lane >= i0 && lane < i0 + kTokensPerCta) {
+    if (t < p.T && lane >= i0 && lane < i0 + TPC) {
         int32_t *dst = p.pos + ((int64_t)s * p.T + t) * p.W;
         for (int r = 0; r < p.W; ++r) dst[r] = spos[lane][r];
     }
@@ -141,12 +147,13 @@ __device__ __forceinline__ void token_metadata(const DispatchParams &p, int s, i
 
 // The last CTA of source s posts (s -> r) for every r, zero-count pairs
 // included, after all of s's rows are stored.
+template <int TPC>
 __device__ __forceinline__ void notify_source_done(const DispatchParams &p, int s) {
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
         const uint32_t tk = atom_add_acq_rel_gpu(p.words + kWordSrcDone + s, 1u);
-        if (tk == (uint32_t)(p.nch * kCtasPerChunk) - 1u) {
+        if (tk == (uint32_t)(p.nch * (kChunk / TPC)) - 1u) {
             p.words[kWordSrcDone + s] = 0u;
             for (int r = 0; r < p.W; ++r)
                 st_release_gpu(p.dflags + r * p.W + s, p.epoch);
@@ -179,22 +186,23 @@ __device__ __forceinline__ uint32_t quant4(const float *f, float scale) {
 
 // ------------------------------------------------------------ register path
 
-template <bool FP8, int U>
+template <bool FP8, int U, int TPC>
 __global__ void __launch_bounds__(kDispatchThreads)
 dispatch_kernel(const DispatchParams p) {
+    constexpr int kCtasPerChunk = kChunk / TPC;
     __shared__ DispatchSmem sm;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int g = blockIdx.x / kCtasPerChunk;
-    const int i0 = (blockIdx.x - g * kCtasPerChunk) * kTokensPerCta;
+    const int i0 = (blockIdx.x - g * kCtasPerChunk) * TPC;
     const int s = g / p.nch;
     const int t0 = (g - s * p.nch) * kChunk;
     const int n_s = p.nt.n[s];
 
-    if (warp == 0) chunk_slots(p, g, s, t0, n_s, i0, sm.pos, sm.mask);
+    if (warp == 0) chunk_slots<TPC>(p, g, s, t0, n_s, i0, sm.pos, sm.mask);
     __syncthreads();
 
-    for (int i = i0 + warp; i < i0 + kTokensPerCta; i += kDispatchWarps) {
+    for (int i = i0 + warp; i < i0 + TPC; i += kDispatchWarps) {
         const int t = t0 + i;
         if (t >= n_s) break;
         const uint32_t m = sm.mask[i];
@@ -292,7 +300,7 @@ dispatch_kernel(const DispatchParams p) {
         }
     }
 
-    if (p.notify) notify_source_done(p, s);
+    if (p.notify) notify_source_done<TPC>(p, s);
 }
 
 // ---------------------------------------------------------------- bulk path
@@ -375,9 +383,10 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-template <int STAGES>
+template <int STAGES, int TPC>
 __global__ void __launch_bounds__(kDispatchThreads)
 dispatch_bulk_kernel(const DispatchParams p) {
+    constexpr int kCtasPerChunk = kChunk / TPC;
     extern __shared__ __align__(128) unsigned char stage_buf[];
     __shared__ BulkSmem sm;
     __shared__ __align__(8) uint64_t bar[STAGES];
@@ -385,17 +394,17 @@ dispatch_bulk_kernel(const DispatchParams p) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int g = blockIdx.x / kCtasPerChunk;
-    const int i0 = (blockIdx.x - g * kCtasPerChunk) * kTokensPerCta;
+    const int i0 = (blockIdx.x - g * kCtasPerChunk) * TPC;
     const int s = g / p.nch;
     const int t0 = (g - s * p.nch) * kChunk;
     const int n_s = p.nt.n[s];
 
     if (warp == 0) {
-        chunk_slots(p, g, s, t0, n_s, i0, sm.pos, sm.mask);
+        chunk_slots<TPC>(p, g, s, t0, n_s, i0, sm.pos, sm.mask);
         __syncwarp();
         if (lane == 0) {
             int n = 0;
-            for (int i = i0; i < i0 + kTokensPerCta; ++i)
+            for (int i = i0; i < i0 + TPC; ++i)
                 if (t0 + i < n_s && sm.mask[i]) sm.list[n++] = i;
             s_n = n;
             for (int i = 0; i < STAGES; ++i) mbar_init(&bar[i], 1);
@@ -467,7 +476,7 @@ dispatch_bulk_kernel(const DispatchParams p) {
         }
     }
 
-    if (p.notify) notify_source_done(p, s);
+    if (p.notify) notify_source_done<TPC>(p, s);
 }
 
 __global__ void dispatch_recv_kernel(uint32_t *dflags, uint32_t *words,
@@ -483,26 +492,56 @@ __global__ void dispatch_recv_kernel(uint32_t *dflags, uint32_t *words,
     if (tid < W) recv_count[tid] = totals[tid];
 }
 
-template <bool FP8, int U>
+template <bool FP8, int U, int TPC>
 cudaError_t launch_dispatch_t(const Config &c, const DispatchParams &p,
                               cudaStream_t st) {
-    dispatch_kernel<FP8, U><<<c.G * kCtasPerChunk, kDispatchThreads, 0, st>>>(p);
+    dispatch_kernel<FP8, U, TPC><<<c.G * (kChunk / TPC), kDispatchThreads, 0, st>>>(p);
     return cudaGetLastError();
 }
 
-template <int STAGES>
+// The ring never needs more stages than the CTA has tokens.
+constexpr int kBulkStages =
+    EP_DISPATCH_BULK_STAGES < EP_DISPATCH_TPC ? EP_DISPATCH_BULK_STAGES : EP_DISPATCH_TPC;
+
+// Residency cap: when a CTA moves a lot of data (its tokens x up to
+// min(W,k) destinations x the row, >= 64 KB), fewer bulk-copy CTAs per SM --
+// fewer concurrent row streams per SM -- measured faster than filling every
+// slot, so the dynamic shared memory is padded until at most
+// EP_DISPATCH_BULK_CTAS_PER_SM CTAs fit.  Small rows or few destinations
+// keep full residency (per-CTA set-up would dominate otherwise).
+template <int STAGES, int TPC>
 cudaError_t launch_dispatch_bulk(const Config &c, const DispatchParams &p,
                                  cudaStream_t st) {
-    const size_t dyn = (size_t)STAGES * c.nvec * 16;
-    static size_t configured = 48 * 1024;     // per instantiation
-    if (dyn > configured) {
+    static size_t configured = 0;       // per instantiation
+    static long share = -1;             // smem per CTA at the capped residency
+    const size_t row = (size_t)c.nvec * 16;
+    size_t dyn = (size_t)STAGES * row;
+    const size_t per_cta = (size_t)TPC * (size_t)(c.W < c.k ? c.W : c.k) * row;
+    if (EP_DISPATCH_BULK_CTAS_PER_SM > 0 && per_cta >= 64 * 1024) {
+        if (share < 0) {
+            int dev = 0, per_sm = 0, reserved = 0;
+            cudaFuncAttributes fa;
+            if (cudaGetDevice(&dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                       dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock,
+                                       dev) != cudaSuccess ||
+                cudaFuncGetAttributes(&fa, dispatch_bulk_kernel<STAGES, TPC>) != cudaSuccess)
+                return cudaGetLastError();
+            const long v = (long)per_sm / EP_DISPATCH_BULK_CTAS_PER_SM - reserved -
+                           (long)fa.sharedSizeBytes;
+            share = v > 0 ? (v & ~127L) : 0;
+        }
+        if ((size_t)share > dyn) dyn = (size_t)share;
+    }
+    if (dyn > configured) {             // opt in to the dynamic size
         const cudaError_t e = cudaFuncSetAttribute(
-            dispatch_bulk_kernel<STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            dispatch_bulk_kernel<STAGES, TPC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
             (int)dyn);
         if (e != cudaSuccess) return e;
         configured = dyn;
     }
-    dispatch_bulk_kernel<STAGES><<<c.G * kCtasPerChunk, kDispatchThreads, dyn, st>>>(p);
+    dispatch_bulk_kernel<STAGES, TPC><<<c.G * (kChunk / TPC), kDispatchThreads, dyn, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -533,12 +572,13 @@ cudaError_t launch_dispatch(const Config &c, const Workspace &ws,
     p.epoch = a.epoch;
     p.timeout_ns = c.timeout_ns;
     p.nt = a.nt;
-    if (c.fp8) return launch_dispatch_t<true, EP_DISPATCH_FP8_UNROLL>(c, p, st);
+    if (c.fp8)
+        return launch_dispatch_t<true, EP_DISPATCH_FP8_UNROLL, EP_DISPATCH_REG_TPC>(c, p, st);
 #if EP_DISPATCH_BULK_STAGES > 0
-    if ((size_t)EP_DISPATCH_BULK_STAGES * c.nvec * 16 <= 160 * 1024)
-        return launch_dispatch_bulk<EP_DISPATCH_BULK_STAGES>(c, p, st);
+    if ((size_t)kBulkStages * c.nvec * 16 <= 160 * 1024)
+        return launch_dispatch_bulk<kBulkStages, EP_DISPATCH_TPC>(c, p, st);
 #endif
-    return launch_dispatch_t<false, EP_DISPATCH_UNROLL>(c, p, st);
+    return launch_dispatch_t<false, EP_DISPATCH_UNROLL, EP_DISPATCH_REG_TPC>(c, p, st);
 }
 
 cudaError_t launch_dispatch_recv(const Config &c, const Workspace &ws,
