@@ -157,3 +157,15 @@ def ragged_num_tokens(wl: Workload, seed: int = 1) -> np.ndarray:
     if W > 1:
         nt[W - 1] = 0
     return nt
+
+
+def draw_fp8_payload(wl: Workload, seed: int = 7):
+    """A pre-quantised FP8 payload for the pass-through dispatch: random
+    E4M3 codes (both NaN patterns excluded) [W][T][H] and positive fp32
+    block scales [W][T][H/128] (log-uniform over 2^-20 .. 2^4)."""
+    W, T, H = wl.world_size, wl.max_tokens_per_rank, wl.hidden
+    rng = np.random.default_rng(np.random.PCG64(seed))
+    codes = rng.integers(0, 254, size=(W, T, H)).astype(np.uint8)
+    codes[codes >= 0x7F] += 1          # 0..126, 128..254: skips 0x7F and 0xFF
+    scales = np.exp2(rng.uniform(-20.0, 4.0, size=(W, T, H // 128))).astype(np.float32)
+    return codes, scales

@@ -77,6 +77,11 @@ def _declare(L):
         "or_identity_rows": (_I, [_I, _I, _I, _I, _I, _P, _I, _P, _P, _P,
                                   _P, _P]),
         "or_combine_gathered": (_I, [_I, _I, _P, _P]),
+        "or_dispatch_prequant": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P,
+                                      _P, _P, _P, _P, _P, _P]),
+        "or_identity_expert_f32": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
+                                        _P, _P]),
+        "or_combine_f32": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
         "or_combine": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
         "or_combine_tokens": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _I,
                                    _P, _P]),
@@ -283,6 +288,50 @@ def combine_tokens(wl, pos, y, w_in, cap, tokens):
                             _p(_c(pos, np.int32)), _p(_c(y, np.uint16)),
                             _p(None if w_in is None else _c(w_in, np.float32)),
                             _p(tokens), n, _p(out), _p(out_w))
+    return out, out_w
+
+
+def dispatch_prequant(wl, x8, scales, w, idx, num_tokens, pos, cap):
+    """Dispatch of pre-quantised FP8 input (codes + block scales copied)."""
+    W, T, H, k = wl.world_size, wl.max_tokens_per_rank, wl.hidden, wl.topk
+    nb = H // 128
+    out = np.zeros((W, cap, H), np.uint8)
+    osc = np.zeros((W, cap, nb), np.float32)
+    ow = np.zeros((W, cap, k), np.float32)
+    oi = np.zeros((W, cap, k), np.int32)
+    sp = np.zeros((W, cap), np.int32)
+    lib().or_dispatch_prequant(W, k, T, H, cap, _p(_c(x8, np.uint8)),
+                               _p(_c(scales, np.float32)), _p(_c(w, np.float32)),
+                               _p(_c(idx, np.int32)), _p(_c(num_tokens, np.int32)),
+                               _p(_c(pos, np.int32)), _p(out), _p(osc), _p(ow),
+                               _p(oi), _p(sp))
+    return dict(out=out, out_scales=osc, out_w=ow, out_idx=oi, src_pos=sp)
+
+
+def identity_expert_f32(wl, recv_count, payload, scales, out_w, out_idx, cap,
+                        fp8=None):
+    """Identity-expert output as fp32 rows [W][cap][H] (no bf16 rounding)."""
+    W, H, k = wl.world_size, wl.hidden, wl.topk
+    fp8 = wl.fp8 if fp8 is None else fp8
+    y = np.zeros((W, cap, H), np.float32)
+    sc = (_c(scales, np.float32) if fp8 else np.zeros((W, cap, 1), np.float32))
+    pl = _c(payload, np.uint8 if fp8 else np.uint16)
+    lib().or_identity_expert_f32(W, wl.num_experts, k, H, cap, int(fp8),
+                                 _p(_c(recv_count, np.int32)), _p(pl), _p(sc),
+                                 _p(_c(out_w, np.float32)),
+                                 _p(_c(out_idx, np.int32)), _p(y))
+    return y
+
+
+def combine_f32(wl, num_tokens, pos, y, w_in, cap):
+    """Combine of fp32 expert rows y [W][cap][H] -> bf16 out [W][T][H]."""
+    W, T, H, k = wl.world_size, wl.max_tokens_per_rank, wl.hidden, wl.topk
+    out = np.zeros((W, T, H), np.uint16)
+    out_w = np.zeros((W, T, k), np.float32) if w_in is not None else None
+    lib().or_combine_f32(W, k, T, H, cap, _p(_c(num_tokens, np.int32)),
+                         _p(_c(pos, np.int32)), _p(_c(y, np.float32)),
+                         _p(None if w_in is None else _c(w_in, np.float32)),
+                         _p(out), _p(out_w))
     return out, out_w
 
 

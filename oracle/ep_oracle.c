@@ -470,3 +470,105 @@ int or_combine_tokens(int W, int k, int T, int H, int cap, const int32_t *pos,
     }
     return OR_OK;
 }
+
+/* ------------------------------------------- pre-quantised FP8 dispatch */
+
+/* Dispatch of an input that is already quantised (the pages' dispatch takes
+ * `scales` next to `input`; the HIP backend "can carry already-quantized
+ * FP8 payloads"): the E4M3 codes x8[s][t][0..H) and the block scales
+ * sc[s][t][0..H/128) of each present token are copied unchanged to every
+ * destination slot p = pos[s][t][r] < cap, with the weights, ids and
+ * src_pos as in or_dispatch.  out uint8 [W][cap][H], out_scales
+ * [W][cap][H/128]. */
+int or_dispatch_prequant(int W, int k, int T, int H, int cap,
+                         const uint8_t *x8, const float *sc, const float *w,
+                         const int32_t *idx, const int32_t *num_tokens,
+                         const int32_t *pos, uint8_t *out, float *out_scales,
+                         float *out_w, int32_t *out_idx, int32_t *src_pos)
+{
+    int nb = H / 128;
+    for (int s = 0; s < W; ++s)
+        for (int t = 0; t < num_tokens[s]; ++t) {
+            int64_t tok = (int64_t)s * T + t;
+            for (int r = 0; r < W; ++r) {
+                int32_t p = pos[tok * W + r];
+                if (p < 0 || p >= cap) continue;
+                int64_t rp = (int64_t)r * cap + p;
+                for (int h = 0; h < H; ++h) out[rp * H + h] = x8[tok * H + h];
+                for (int b = 0; b < nb; ++b) out_scales[rp * nb + b] = sc[tok * nb + b];
+                for (int j = 0; j < k; ++j) {
+                    out_w[rp * k + j] = w[tok * k + j];
+                    out_idx[rp * k + j] = idx[tok * k + j];
+                }
+                src_pos[rp] = s * T + t;
+            }
+        }
+    return OR_OK;
+}
+
+/* ------------------------------------------------ FP32 combine input */
+
+/* Identity expert with an fp32 output row (the expert hands combine fp32
+ * rows): y[h] = fl32(v_h * alpha), alpha and v as in identity_row, with no
+ * rounding to bf16.  y is float [W][cap][H]. */
+int or_identity_expert_f32(int W, int E, int k, int H, int cap, int fp8,
+                           const int32_t *recv_count, const void *payload,
+                           const float *scales, const float *out_w,
+                           const int32_t *out_idx, float *y)
+{
+    int Er = E / W;
+    int nb = fp8 ? H / 128 : 0;
+    for (int r = 0; r < W; ++r) {
+        int n = recv_count[r] < cap ? recv_count[r] : cap;
+        for (int p = 0; p < n; ++p) {
+            int64_t rp = (int64_t)r * cap + p;
+            float alpha = 0.0f;
+            for (int j = 0; j < k; ++j)
+                if (out_idx[rp * k + j] / Er == r)
+                    alpha = alpha + out_w[rp * k + j];
+            for (int h = 0; h < H; ++h) {
+                float v;
+                if (fp8)
+                    v = or_e4m3_value(((const uint8_t *)payload)[rp * H + h]) *
+                        scales[rp * nb + h / 128];
+                else
+                    v = or_bf16_to_f32(((const uint16_t *)payload)[rp * H + h]);
+                y[rp * H + h] = v * alpha;
+            }
+        }
+    }
+    return OR_OK;
+}
+
+/* Combine of fp32 expert rows: out[s][t][h] = bf16_rne(+0.0f + y_r0[p0][h]
+ * + y_r1[p1][h] + ...) over r in D(s,t) ascending (slots < cap), each '+'
+ * an fp32 add; out_w as in or_combine.  y float [W][cap][H]. */
+int or_combine_f32(int W, int k, int T, int H, int cap, const int32_t *num_tokens,
+                   const int32_t *pos, const float *y, const float *w_in,
+                   uint16_t *out, float *out_w)
+{
+    for (int s = 0; s < W; ++s)
+        for (int t = 0; t < num_tokens[s]; ++t) {
+            int64_t tok = (int64_t)s * T + t;
+            for (int h = 0; h < H; ++h) {
+                float acc = 0.0f;
+                for (int r = 0; r < W; ++r) {
+                    int32_t p = pos[tok * W + r];
+                    if (p < 0 || p >= cap) continue;
+                    acc = acc + y[((int64_t)r * cap + p) * H + h];
+                }
+                out[tok * H + h] = or_bf16_rne(acc);
+            }
+            if (w_in && out_w)
+                for (int j = 0; j < k; ++j) {
+                    float acc = 0.0f;
+                    for (int r = 0; r < W; ++r) {
+                        int32_t p = pos[tok * W + r];
+                        if (p < 0 || p >= cap) continue;
+                        acc = acc + w_in[((int64_t)r * cap + p) * k + j];
+                    }
+                    out_w[tok * k + j] = acc;
+                }
+        }
+    return OR_OK;
+}

@@ -128,3 +128,50 @@ def combine(disp, ys, w_in, W, T, H, k, num_tokens):
             out[(s, t)] = torch_bf16_bits(acc)
             out_w[(s, t)] = accw
     return out, out_w
+
+
+def dispatch_prequant(x8, sc, w, idx, num_tokens, W, E):
+    """Pre-quantised payload: per rank, the received codes and scales rows."""
+    T = x8.shape[1]
+    res = {}
+    for r, rows in receive_lists(idx, num_tokens, W, E).items():
+        res[r] = dict(rows=rows,
+                      out=np.array([x8[s, t] for s, t in rows]).reshape(-1, x8.shape[2]),
+                      out_scales=np.array([sc[s, t] for s, t in rows],
+                                          np.float32).reshape(-1, sc.shape[2]),
+                      src_pos=np.array([s * T + t for s, t in rows], np.int32))
+    return res
+
+
+def identity_expert_f32(d, r, W, E, fp8=False):
+    """fp32 rows f32(v * alpha) of rank r (no bf16 rounding)."""
+    Er = E // W
+    ys = []
+    for i in range(len(d["rows"])):
+        alpha = np.float32(0)
+        for j in range(d["out_idx"].shape[1]):
+            if int(d["out_idx"][i, j]) // Er == r:
+                alpha = np.float32(alpha + d["out_w"][i, j])
+        if fp8:
+            H = d["out"].shape[1]
+            v = (torch_e4m3_value(d["out"][i]) * np.repeat(d["out_scales"][i], 128)[:H]).astype(np.float32)
+        else:
+            v = to_f32(d["out"][i])
+        ys.append((v * alpha).astype(np.float32))
+    return ys
+
+
+def combine_f32(disp, ys, W, T, H, num_tokens):
+    """out[(s,t)] = bf16(sum over r ascending of the fp32 rows)."""
+    where = {}
+    for r in range(W):
+        for i, st in enumerate(disp[r]["rows"]):
+            where.setdefault(st, []).append((r, i))
+    out = {}
+    for s in range(W):
+        for t in range(int(num_tokens[s])):
+            acc = np.zeros(H, np.float32)
+            for r, i in sorted(where.get((s, t), [])):
+                acc = (acc + ys[r][i]).astype(np.float32)
+            out[(s, t)] = torch_bf16_bits(acc)
+    return out

@@ -468,3 +468,86 @@ def test_sampled_row_functions_agree_with_whole_buffer_functions():
                     if res["pos"][s, t, r] >= 0]
             assert np.array_equal(oracle.combine_gathered(np.array(rows)),
                                   res["combined"][s, t])
+
+
+# ------------------------------------------- pre-quantised FP8, fp32 combine
+
+@pytest.mark.parametrize("seed", range(3))
+def test_prequant_dispatch_matches_bruteforce(seed):
+    rng = np.random.default_rng(700 + seed)
+    wl, inp = _random_case(rng, 4, 2, 3, 11, 256, fp8=True)
+    x8, sc = gen.draw_fp8_payload(wl, seed=seed)
+    pos, C, rc = oracle.layout(wl, inp.indices, inp.num_tokens)
+    cap = wl.world_size * wl.max_tokens_per_rank
+    d = oracle.dispatch_prequant(wl, x8, sc, inp.weights, inp.indices,
+                                 inp.num_tokens, pos, cap)
+    ref = bf.dispatch_prequant(x8, sc, inp.weights, inp.indices, inp.num_tokens,
+                               wl.world_size, wl.num_experts)
+    for r in range(wl.world_size):
+        n = len(ref[r]["rows"])
+        assert rc[r] == n
+        if n:
+            assert np.array_equal(d["out"][r, :n], ref[r]["out"])
+            assert np.array_equal(d["out_scales"][r, :n].view(np.uint32),
+                                  ref[r]["out_scales"].view(np.uint32))
+        assert np.array_equal(d["src_pos"][r, :n], ref[r]["src_pos"])
+    # quantising first and passing the codes through equals the fused path
+    q, s = oracle.quant_rows(inp.x_bits.reshape(-1, wl.hidden))
+    d2 = oracle.dispatch_prequant(wl, q.reshape(x8.shape), s.reshape(sc.shape),
+                                  inp.weights, inp.indices, inp.num_tokens, pos, cap)
+    fused = oracle.dispatch(wl, inp.x_bits, inp.weights, inp.indices,
+                            inp.num_tokens, pos, cap)
+    for r in range(wl.world_size):
+        assert np.array_equal(d2["out"][r, :rc[r]], fused["out"][r, :rc[r]])
+        assert np.array_equal(d2["out_scales"][r, :rc[r]], fused["out_scales"][r, :rc[r]])
+
+
+def test_payload_draw_has_no_nan_codes():
+    wl = gen.Workload("p", 2, 4, 2, 16, 256, fp8=True)
+    x8, sc = gen.draw_fp8_payload(wl)
+    assert not np.any((x8 & 0x7F) == 0x7F)
+    assert np.all(sc > 0) and np.all(np.isfinite(oracle.e4m3_value(x8)))
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_fp32_combine_matches_bruteforce(fp8):
+    rng = np.random.default_rng(800 + int(fp8))
+    wl, inp = _random_case(rng, 5, 2, 4, 9, 256, fp8=fp8)
+    res = oracle.run_all(inp)
+    W, E, T, H = wl.world_size, wl.num_experts, wl.max_tokens_per_rank, wl.hidden
+    cap = res["cap"]
+    y32 = oracle.identity_expert_f32(wl, res["recv_count"], res["out"],
+                                     res["out_scales"], res["out_w"],
+                                     res["out_idx"], cap)
+    # rounding the fp32 identity rows to bf16 gives the (pinned) bf16 rows
+    for r in range(W):
+        n = res["recv_count"][r]
+        assert np.array_equal(bf.torch_bf16_bits(y32[r, :n]), res["y"][r, :n])
+    disp = bf.dispatch(inp.x_bits, inp.weights, inp.indices, inp.num_tokens,
+                       W, E, fp8=fp8)
+    ys = {r: bf.identity_expert_f32(disp[r], r, W, E, fp8=fp8) for r in range(W)}
+    for r in range(W):
+        for i in range(len(ys[r])):
+            assert np.array_equal(ys[r][i].view(np.uint32), y32[r, i].view(np.uint32))
+    # wide-range fp32 rows: the ordered fp32 sum
+    mag = 2.0 ** rng.integers(-30, 31, size=y32.shape)
+    yw = (rng.standard_normal(y32.shape) * mag).astype(np.float32)
+    ysw = {r: [yw[r, i] for i in range(len(disp[r]["rows"]))] for r in range(W)}
+    exp = bf.combine_f32(disp, ysw, W, T, H, inp.num_tokens)
+    got, _ = oracle.combine_f32(wl, inp.num_tokens, res["pos"], yw, None, cap)
+    for (s, t), row in exp.items():
+        assert np.array_equal(got[s, t], row)
+
+
+def test_fp32_combine_order_is_ascending_rank():
+    W = 3
+    wl = gen.Workload("order32", W, W, W, 1, 8)
+    idx = np.array([[[0, 1, 2]], [[0, 1, 2]], [[0, 1, 2]]], np.int32)
+    nt = np.array([1, 0, 0], np.int32)
+    pos, _, _ = oracle.layout(wl, idx, nt)
+    y = np.zeros((W, W, 8), np.float32)
+    y[0, 0] = 1.0
+    y[1, 0] = 2.0 ** -24
+    y[2, 0] = -1.0
+    out, _ = oracle.combine_f32(wl, nt, pos, y, None, W)
+    assert np.all(out[0, 0] == 0)
