@@ -55,22 +55,28 @@ def parse():
                     help="override T (tokens per rank), e.g. for a profiling case")
     ap.add_argument("--cap", type=int, default=0,
                     help="receive rows per rank (0: W*T)")
+    ap.add_argument("--fp8-input", action="store_true",
+                    help="FP8 workloads: dispatch a pre-quantised payload (codes + scales)")
+    ap.add_argument("--combine-dtype", choices=["bf16", "fp32"], default="bf16",
+                    help="element type of the expert rows combine reads")
     return ap.parse_args()
 
 
 # ------------------------------------------------------------- bookkeeping
 
-def algorithmic_bytes(wl, P, N, fp8, with_weights=True):
+def algorithmic_bytes(wl, P, N, fp8, with_weights=True, fp8_input=False,
+                      y_bytes=2):
     """Bytes the method must move (each counted once).
-    dispatch: read N*(H*2 + 8k) [row once + ids + weights];
-              write P*(H*b + s_b + 8k + 4) [row, scales, weights, ids, src_pos]
-    combine:  read P*H*2 (+ P*4k weights); write N*H*2 (+ N*4k)."""
+    dispatch: read N*(H*b_in + s_in + 8k) [row once (+ its scales) + ids +
+              weights]; write P*(H*b + s_b + 8k + 4) [row, scales, weights,
+              ids, src_pos]
+    combine:  read P*H*y_bytes (+ P*4k weights); write N*H*2 (+ N*4k)."""
     H, k = wl.hidden, wl.topk
     b_out = 1 if fp8 else 2
     s_b = 4 * (H // 128) if fp8 else 0
-    d_read = N * (H * 2 + 8 * k)
+    d_read = N * ((H + s_b) if fp8_input else H * 2) + N * 8 * k
     d_write = P * (H * b_out + s_b + 8 * k + 4)
-    c_read = P * H * 2 + (P * 4 * k if with_weights else 0)
+    c_read = P * H * y_bytes + (P * 4 * k if with_weights else 0)
     c_write = N * H * 2 + (N * 4 * k if with_weights else 0)
     return dict(dispatch=d_read + d_write, combine=c_read + c_write,
                 dispatch_read=d_read, dispatch_write=d_write,
@@ -200,11 +206,19 @@ def run_ours(args, rank, world, local_rank):
     P = int(sum(len(set((inp.indices[s, t] // Er).tolist()))
                 for s in range(W) for t in range(T)))
 
+    if args.fp8_input and not wl.fp8:
+        raise SystemExit("--fp8-input needs an FP8 workload")
     cfg = EpDispatchCombineConfig(W, wl.num_experts, k, H, T,
                                   max_recv_tokens_per_rank=args.cap,
-                                  dispatch_dtype="fp8_e4m3" if wl.fp8 else "bf16")
+                                  dispatch_dtype="fp8_e4m3" if wl.fp8 else "bf16",
+                                  combine_dtype=args.combine_dtype)
     op = EpDispatchCombineOp(cfg, device=dev)
     x = torch.from_numpy(inp.x_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    xsc = None
+    if args.fp8_input:        # pre-quantised payload: E4M3 codes + block scales
+        x8, sc8 = gen.draw_fp8_payload(wl)
+        x = torch.from_numpy(x8).to(dev)
+        xsc = torch.from_numpy(sc8).to(dev)
     w = torch.from_numpy(inp.weights).to(dev)
     idx = torch.from_numpy(inp.indices).to(dev)
     out = torch.empty((W, T, H), dtype=torch.bfloat16, device=dev)
@@ -215,13 +229,18 @@ def run_ours(args, rank, world, local_rank):
     # identity expert fills the registered combine buffer (not timed) and
     # the combined output must give back the input
     with torch.cuda.stream(stream):
-        op.dispatch(x, w, None, idx, num_tokens=nt, stream=stream)
+        op.dispatch(x, w, xsc, idx, num_tokens=nt, stream=stream)
         op.identity_expert(stream=stream)
         op.combine(weights=op.out_w, out=out, out_weights=out_w, stream=stream)
     stream.synchronize()
-    xs = x.float()
+    if xsc is not None:       # expected: the dequantised payload
+        xs = x.view(torch.float8_e4m3fn).float() * xsc.repeat_interleave(128, dim=2)
+    else:
+        xs = x.float()
     ys = out.float()
-    if wl.fp8:
+    if xsc is not None:
+        ident_ok = bool(((ys - xs).abs() <= xs.abs() * (2.0 ** -8 * 10) + 1e-30).all())
+    elif wl.fp8:
         ident_ok = bool(((ys - xs).abs() <= xs.abs() * 0.07 + 1e-2).all())
     else:
         ident_ok = bool(((ys - xs).abs() <= xs.abs() * (2.0 ** -8 * 10)).all())
@@ -235,7 +254,7 @@ def run_ours(args, rank, world, local_rank):
         op.layout(idx, num_tokens=nt, stream=stream)
         if ev is not None:
             ev[1].record(stream)
-        op.dispatch_send_replay(x, w, idx, num_tokens=nt, stream=stream)
+        op.dispatch_send_replay(x, w, idx, num_tokens=nt, stream=stream, scales=xsc)
         op.dispatch_recv(stream=stream)
         if ev is not None:
             ev[2].record(stream)
@@ -282,7 +301,8 @@ def run_ours(args, rank, world, local_rank):
     ms_per_step = total_ms / args.steps
     value = world * N / (ms_per_step / 1e3)
 
-    ab = algorithmic_bytes(wl, P, N, wl.fp8)
+    ab = algorithmic_bytes(wl, P, N, wl.fp8, fp8_input=args.fp8_input,
+                           y_bytes=4 if args.combine_dtype == "fp32" else 2)
     step_bytes = ab["dispatch"] + ab["combine"]
     peak, peak_kind = measured_peak()
     d_ms, c_ms = float(dis.mean()), float(com.mean())
@@ -290,22 +310,27 @@ def run_ours(args, rank, world, local_rank):
     dom_ms = c_ms if dominant == "combine" else d_ms
     achieved = ab[dominant] / (dom_ms / 1e3) / 1e9
     kname = ("combine_kernel" if dominant == "combine"
-             else ("dispatch_kernel" if wl.fp8 else "dispatch_bulk_kernel"))
+             else ("dispatch_kernel" if wl.fp8 and not args.fp8_input
+                   else "dispatch_bulk_kernel"))
 
     # end to end: pinned host inputs -> device, path, combined output -> host
     e2e = None
     if args.e2e_steps > 0:
-        hx = torch.from_numpy(inp.x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hx = x.cpu().pin_memory()
+        hsc = None if xsc is None else xsc.cpu().pin_memory()
         hw = torch.from_numpy(inp.weights).pin_memory()
         hi = torch.from_numpy(inp.indices).pin_memory()
         hout = torch.empty((W, T, H), dtype=torch.bfloat16).pin_memory()
         dx, dw, di = torch.empty_like(x), torch.empty_like(w), torch.empty_like(idx)
+        dsc = None if xsc is None else torch.empty_like(xsc)
 
         def e2e_step():
             dx.copy_(hx, non_blocking=True)
+            if dsc is not None:
+                dsc.copy_(hsc, non_blocking=True)
             dw.copy_(hw, non_blocking=True)
             di.copy_(hi, non_blocking=True)
-            op.dispatch(dx, dw, None, di, num_tokens=nt, stream=stream)
+            op.dispatch(dx, dw, dsc, di, num_tokens=nt, stream=stream)
             op.combine(weights=op.out_w, out=out, out_weights=out_w, stream=stream)
             hout.copy_(out, non_blocking=True)
 
@@ -328,7 +353,8 @@ def run_ours(args, rank, world, local_rank):
             t = torch.tensor([e_ms], device=dev)
             torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
             e_ms = float(t.item())
-        h2d = hx.numel() * 2 + hw.numel() * 4 + hi.numel() * 4
+        h2d = hx.numel() * hx.element_size() + hw.numel() * 4 + hi.numel() * 4 + \
+            (0 if hsc is None else hsc.numel() * 4)
         d2h = hout.numel() * 2
         e2e = {"value": world * N / (e_ms / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -354,8 +380,10 @@ def run_ours(args, rank, world, local_rank):
         "config": {
             "workload": f"{wl.name}: W={W} logical ranks on one GPU, E={wl.num_experts}, "
                         f"k={k}, T={T} tokens/rank, H={H}, "
-                        f"{'fp8 e4m3' if wl.fp8 else 'bf16'} dispatch, fp32-accumulate "
-                        f"bf16 combine with weights, {wl.routing} routing",
+                        f"{'fp8 e4m3' if wl.fp8 else 'bf16'} dispatch"
+                        f"{' of a pre-quantised payload' if args.fp8_input else ''}, "
+                        f"fp32-accumulate bf16 combine of {args.combine_dtype} expert rows "
+                        f"with weights, {wl.routing} routing",
             "tokens_per_step": N,
             "routed_pairs": P,
             "l2": "every input and output is larger than L2 (x 470 MB, "

@@ -46,7 +46,7 @@ class EpConfigC(ctypes.Structure):
         ("dispatch_dtype", ctypes.c_int32),
         ("early_notify", ctypes.c_int32),
         ("fused_recv", ctypes.c_int32),
-        ("reserved0", ctypes.c_int32),
+        ("combine_dtype", ctypes.c_int32),
         ("wait_timeout_ns", ctypes.c_int64),
     ]
 
@@ -85,7 +85,7 @@ SIGNATURES = {
     "ep_dispatch_send": (_S, [_P, _P, _P, _P, _P, _P, _P]),
     "ep_dispatch_recv": (_S, [_P, _P]),
     "ep_dispatch": (_S, [_P, _P, _P, _P, _P, _P, _P]),
-    "ep_dispatch_send_replay": (_S, [_P, _P, _P, _P, _P, _P]),
+    "ep_dispatch_send_replay": (_S, [_P, _P, _P, _P, _P, _P, _P]),
     "ep_dispatch_outputs": (_S, [_P, ctypes.POINTER(EpDispatchOutC)]),
     "ep_get_combine_input_buffer": (_S, [_P, _I32, ctypes.POINTER(_P), ctypes.POINTER(_I64)]),
     "ep_combine_send": (_S, [_P, _P]),

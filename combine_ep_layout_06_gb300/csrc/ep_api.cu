@@ -38,6 +38,8 @@ ep_status_t make_config(const ep_config_t *in, Config *c) {
     if (in->dispatch_dtype != EP_DT_BF16 && in->dispatch_dtype != EP_DT_FP8_E4M3)
         return EP_ERR_INVALID_ARGS;
     const bool fp8 = in->dispatch_dtype == EP_DT_FP8_E4M3;
+    if (in->combine_dtype != EP_DT_BF16 && in->combine_dtype != EP_DT_FP32)
+        return EP_ERR_INVALID_ARGS;
     if (fp8 && (H % EP_QUANT_BLOCK != 0 || H > 16384)) return EP_ERR_INVALID_ARGS;
     const int64_t cap = in->max_recv_tokens_per_rank > 0
                             ? in->max_recv_tokens_per_rank
@@ -48,6 +50,7 @@ ep_status_t make_config(const ep_config_t *in, Config *c) {
     c->W = W; c->E = E; c->Er = E / W; c->k = k; c->H = H; c->T = T;
     c->cap = (int)cap;
     c->fp8 = fp8;
+    c->y_f32 = in->combine_dtype == EP_DT_FP32;
     c->nch = (T + kChunk - 1) / kChunk;
     c->G = W * c->nch;
     c->Q = (c->G + kGroup - 1) / kGroup;
@@ -113,7 +116,7 @@ void plan_workspace(const Config &c, char *base, Workspace *ws) {
     ws->off_w = seg_take(cap * k * 4);
     ws->off_idx = seg_take(cap * k * 4);
     ws->off_src = seg_take(cap * 4);
-    ws->off_comb = seg_take(cap * H * 2);
+    ws->off_comb = seg_take(cap * H * (c.y_f32 ? 4 : 2));
     ws->seg_stride = (int64_t)so;
     ws->seg0 = base ? base + off : nullptr;
     ws->total_bytes = off + so * W;
@@ -221,14 +224,16 @@ static ep_status_t check_dispatch_args(ep_handle_t *h, const void *d_x,
                                        const float *d_w, const float *d_scales,
                                        const int32_t *d_idx) {
     if (!h || !d_x || !d_w || !d_idx) return EP_ERR_INVALID_ARGS;
-    if (d_scales) return EP_ERR_INVALID_ARGS;   // pre-quantised input: not accepted
+    // pre-quantised input (codes + block scales) needs an FP8 dispatch
+    if (d_scales && (!h->cfg.fp8 || !aligned(d_scales, 16))) return EP_ERR_INVALID_ARGS;
     if (!aligned(d_x, 16) || !aligned(d_w, 4) || !aligned(d_idx, 4))
         return EP_ERR_INVALID_ARGS;
     return EP_SUCCESS;
 }
 
 static ep_status_t dispatch_send_impl(ep_handle_t *h, const void *d_x,
-                                      const float *d_w, const int32_t *d_idx,
+                                      const float *d_w, const float *d_scales,
+                                      const int32_t *d_idx,
                                       const TokenCounts &nt, bool run_layout,
                                       bool publish, cudaStream_t st) {
     if (h->cfg.early_notify) ++h->dispatch_epoch;
@@ -241,6 +246,7 @@ static ep_status_t dispatch_send_impl(ep_handle_t *h, const void *d_x,
     }
     DispatchArgs a;
     a.x = d_x;
+    a.scales_in = d_scales;
     a.w = d_w;
     a.idx = d_idx;
     a.nt = nt;
@@ -257,7 +263,7 @@ ep_status_t ep_dispatch_send(ep_handle_t *h, const void *d_x, const float *d_w,
     if (!read_counts(h, h_num_tokens, &nt)) return EP_ERR_INVALID_ARGS;
     if (h->dispatch_pending) return EP_ERR_BAD_STATE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    s = dispatch_send_impl(h, d_x, d_w, d_idx, nt, true, false, st);
+    s = dispatch_send_impl(h, d_x, d_w, d_scales, d_idx, nt, true, false, st);
     if (s != EP_SUCCESS) return s;
     s = gpu(h, cudaEventRecord(h->ev_dispatch_sent, st), "cudaEventRecord");
     if (s != EP_SUCCESS) return s;
@@ -266,16 +272,17 @@ ep_status_t ep_dispatch_send(ep_handle_t *h, const void *d_x, const float *d_w,
 }
 
 ep_status_t ep_dispatch_send_replay(ep_handle_t *h, const void *d_x,
-                                    const float *d_w, const int32_t *d_idx,
+                                    const float *d_w, const float *d_scales,
+                                    const int32_t *d_idx,
                                     const int32_t *h_num_tokens, void *stream) {
-    ep_status_t s = check_dispatch_args(h, d_x, d_w, nullptr, d_idx);
+    ep_status_t s = check_dispatch_args(h, d_x, d_w, d_scales, d_idx);
     if (s != EP_SUCCESS) return s;
     TokenCounts nt;
     if (!read_counts(h, h_num_tokens, &nt)) return EP_ERR_INVALID_ARGS;
     if (!h->layout_valid || h->dispatch_pending) return EP_ERR_BAD_STATE;
     if (std::memcmp(&nt, &h->layout_nt, sizeof(nt)) != 0) return EP_ERR_BAD_STATE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    s = dispatch_send_impl(h, d_x, d_w, d_idx, nt, false, false, st);
+    s = dispatch_send_impl(h, d_x, d_w, d_scales, d_idx, nt, false, false, st);
     if (s != EP_SUCCESS) return s;
     s = gpu(h, cudaEventRecord(h->ev_dispatch_sent, st), "cudaEventRecord");
     if (s != EP_SUCCESS) return s;
@@ -310,7 +317,7 @@ ep_status_t ep_dispatch(ep_handle_t *h, const void *d_x, const float *d_w,
     // One stream: the layout publishes recv_count itself unless the ready
     // flags must be checked by a receive step.
     const bool notify = h->cfg.early_notify;
-    s = dispatch_send_impl(h, d_x, d_w, d_idx, nt, true, !notify, st);
+    s = dispatch_send_impl(h, d_x, d_w, d_scales, d_idx, nt, true, !notify, st);
     if (s != EP_SUCCESS) return s;
     if (notify)
         s = gpu(h, launch_dispatch_recv(h->cfg, h->ws, true, h->dispatch_epoch, st),
@@ -342,7 +349,7 @@ ep_status_t ep_dispatch_outputs(const ep_handle_t *h, ep_dispatch_out_t *o) {
 ep_status_t ep_get_combine_input_buffer(const ep_handle_t *h, int32_t dtype,
                                         void **d_ptr, int64_t *rank_stride_bytes) {
     if (!h || !d_ptr || !rank_stride_bytes) return EP_ERR_INVALID_ARGS;
-    if (dtype != EP_DT_BF16) return EP_ERR_NOT_FOUND;
+    if (dtype != (h->cfg.y_f32 ? EP_DT_FP32 : EP_DT_BF16)) return EP_ERR_NOT_FOUND;
     *d_ptr = h->ws.seg0 + h->ws.off_comb;
     *rank_stride_bytes = h->ws.seg_stride;
     return EP_SUCCESS;
@@ -372,7 +379,7 @@ static ep_status_t combine_args(ep_handle_t *h, const void *d_y, int64_t y_strid
     if (!d_out || !aligned(d_out, 16)) return EP_ERR_INVALID_ARGS;
     if (d_idx && !aligned(d_idx, 4)) return EP_ERR_INVALID_ARGS;
     if ((d_w_in == nullptr) != (d_out_w == nullptr)) return EP_ERR_INVALID_ARGS;
-    const int64_t row_bytes = (int64_t)c.cap * c.H * 2;
+    const int64_t row_bytes = (int64_t)c.cap * c.H * (c.y_f32 ? 4 : 2);
     if (d_y) {
         if (y_stride == 0) y_stride = row_bytes;
         if (!aligned(d_y, 16) || y_stride % 16 != 0 || y_stride < row_bytes)
@@ -495,7 +502,7 @@ ep_status_t ep_test_identity_expert(ep_handle_t *h, void *d_y,
                                     int64_t y_rank_stride_bytes, void *stream) {
     if (!h) return EP_ERR_INVALID_ARGS;
     if (!h->layout_valid) return EP_ERR_BAD_STATE;
-    const int64_t row_bytes = (int64_t)h->cfg.cap * h->cfg.H * 2;
+    const int64_t row_bytes = (int64_t)h->cfg.cap * h->cfg.H * (h->cfg.y_f32 ? 4 : 2);
     char *y;
     int64_t ys;
     if (d_y) {

@@ -98,9 +98,18 @@ __device__ void fused_receive_wait(const CombineParams &p) {
     __syncthreads();
 }
 
-template <int MAXD, int U, bool COHERENT>
+__device__ __forceinline__ void add_f32x4(float *acc, const uint4 &v) {
+    acc[0] = acc[0] + __uint_as_float(v.x);
+    acc[1] = acc[1] + __uint_as_float(v.y);
+    acc[2] = acc[2] + __uint_as_float(v.z);
+    acc[3] = acc[3] + __uint_as_float(v.w);
+}
+
+// F32: the expert rows are fp32 (two 16-byte loads per 8 output elements).
+template <int MAXD, int U, bool COHERENT, bool F32>
 __global__ void __launch_bounds__(kCombineThreads, EP_COMBINE_MIN_BLOCKS)
 combine_kernel(const CombineParams p) {
+    constexpr int NL = F32 ? 2 : 1;       // 16-byte loads per output vector
     if (p.fused_wait) fused_receive_wait(p);
 
     const int lane = threadIdx.x & 31;
@@ -136,7 +145,7 @@ combine_kernel(const CombineParams p) {
                 const int r = __ffs(mm) - 1;
                 mm &= mm - 1u;
                 const int slot = __shfl_sync(0xffffffffu, pr, r);
-                rows[j] = p.y + (int64_t)r * p.y_stride + (int64_t)slot * p.nvec * 16;
+                rows[j] = p.y + (int64_t)r * p.y_stride + (int64_t)slot * p.nvec * 16 * NL;
                 nd = j + 1;
             }
         }
@@ -144,16 +153,20 @@ combine_kernel(const CombineParams p) {
 
     uint4 *out_row = reinterpret_cast<uint4 *>(p.out) + tok * p.nvec;
     for (int v0 = lane; v0 < p.nvec; v0 += 32 * U) {
-        uint4 val[U][MAXD];
+        uint4 val[U][MAXD][NL];
 #pragma unroll
         for (int j = 0; j < MAXD; ++j) {
             if (j < nd) {
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int v = v0 + 32 * u;
-                    if (v < p.nvec)
-                        val[u][j] = COHERENT ? ld_coherent16(rows[j] + (int64_t)v * 16)
-                                             : ld_stream16(rows[j] + (int64_t)v * 16);
+                    if (v < p.nvec) {
+#pragma unroll
+                        for (int l = 0; l < NL; ++l) {
+                            const char *a = rows[j] + ((int64_t)v * NL + l) * 16;
+                            val[u][j][l] = COHERENT ? ld_coherent16(a) : ld_stream16(a);
+                        }
+                    }
                 }
             }
         }
@@ -165,8 +178,16 @@ combine_kernel(const CombineParams p) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
 #pragma unroll
-            for (int j = 0; j < MAXD; ++j)
-                if (j < nd) add_bf16x8(acc, val[u][j]);
+            for (int j = 0; j < MAXD; ++j) {
+                if (j < nd) {
+                    if constexpr (F32) {
+                        add_f32x4(acc, val[u][j][0]);
+                        add_f32x4(acc + 4, val[u][j][1]);
+                    } else {
+                        add_bf16x8(acc, val[u][j][0]);
+                    }
+                }
+            }
             uint4 o;
             o.x = pack_bf16x2(acc[0], acc[1]);
             o.y = pack_bf16x2(acc[2], acc[3]);
@@ -206,7 +227,8 @@ __global__ void __launch_bounds__(256)
 identity_expert_kernel(const char *seg0, int64_t seg_stride, int64_t off_out,
                        int64_t off_scales, int64_t off_w, int64_t off_idx,
                        const int32_t *totals, char *y, int64_t y_stride,
-                       int W, int E, int Er, int k, int H, int cap, int fp8) {
+                       int W, int E, int Er, int k, int H, int cap, int fp8,
+                       int y_f32) {
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int r = (int)(gw / cap);
@@ -222,7 +244,8 @@ identity_expert_kernel(const char *seg0, int64_t seg_stride, int64_t off_out,
         if ((uint32_t)e < (uint32_t)E && e / Er == r) alpha = alpha + wrow[j];
     }
     const int nvec = H / 8;
-    uint4 *yrow = reinterpret_cast<uint4 *>(y + (int64_t)r * y_stride) + (int64_t)slot * nvec;
+    uint4 *yrow = reinterpret_cast<uint4 *>(y + (int64_t)r * y_stride) +
+                  (int64_t)slot * nvec * (y_f32 ? 2 : 1);
     for (int v = lane; v < nvec; v += 32) {
         float f[8];
         if (fp8) {
@@ -247,29 +270,44 @@ identity_expert_kernel(const char *seg0, int64_t seg_stride, int64_t off_out,
                 f[2 * i + 1] = __uint_as_float(w4[i] & 0xffff0000u);
             }
         }
-        uint4 o;
-        o.x = pack_bf16x2(f[0] * alpha, f[1] * alpha);
-        o.y = pack_bf16x2(f[2] * alpha, f[3] * alpha);
-        o.z = pack_bf16x2(f[4] * alpha, f[5] * alpha);
-        o.w = pack_bf16x2(f[6] * alpha, f[7] * alpha);
-        yrow[v] = o;
+        if (y_f32) {
+            float g[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) g[e] = f[e] * alpha;
+            yrow[2 * v] = make_uint4(__float_as_uint(g[0]), __float_as_uint(g[1]),
+                                     __float_as_uint(g[2]), __float_as_uint(g[3]));
+            yrow[2 * v + 1] = make_uint4(__float_as_uint(g[4]), __float_as_uint(g[5]),
+                                         __float_as_uint(g[6]), __float_as_uint(g[7]));
+        } else {
+            uint4 o;
+            o.x = pack_bf16x2(f[0] * alpha, f[1] * alpha);
+            o.y = pack_bf16x2(f[2] * alpha, f[3] * alpha);
+            o.z = pack_bf16x2(f[4] * alpha, f[5] * alpha);
+            o.w = pack_bf16x2(f[6] * alpha, f[7] * alpha);
+            yrow[v] = o;
+        }
     }
 }
 
-template <int MAXD, int U, bool COH>
+template <int MAXD, int U, bool COH, bool F32>
 cudaError_t launch_combine_t(const Config &c, const CombineParams &p,
                              cudaStream_t st) {
     const int64_t tokens = (int64_t)c.W * c.T;
     const int blocks = (int)((tokens + kCombineWarps - 1) / kCombineWarps);
-    combine_kernel<MAXD, U, COH><<<blocks, kCombineThreads, 0, st>>>(p);
+    combine_kernel<MAXD, U, COH, F32><<<blocks, kCombineThreads, 0, st>>>(p);
     return cudaGetLastError();
 }
 
 template <int MAXD, int U>
 cudaError_t launch_combine_m(const Config &c, const CombineParams &p,
                              cudaStream_t st) {
-    if (p.fused_wait) return launch_combine_t<MAXD, U, true>(c, p, st);
-    return launch_combine_t<MAXD, U, false>(c, p, st);
+    if (c.y_f32) {
+        constexpr int U32 = U > 1 ? U / 2 : 1;    // twice the bytes per vector
+        if (p.fused_wait) return launch_combine_t<MAXD, U32, true, true>(c, p, st);
+        return launch_combine_t<MAXD, U32, false, true>(c, p, st);
+    }
+    if (p.fused_wait) return launch_combine_t<MAXD, U, true, false>(c, p, st);
+    return launch_combine_t<MAXD, U, false, false>(c, p, st);
 }
 
 }  // namespace
@@ -323,7 +361,7 @@ cudaError_t launch_identity_expert(const Config &c, const Workspace &ws,
     identity_expert_kernel<<<blocks, 256, 0, st>>>(
         ws.seg0, ws.seg_stride, ws.off_out, ws.off_scales, ws.off_w, ws.off_idx,
         ws.group_base + (int64_t)c.Q * c.W, y, y_stride, c.W, c.E, c.Er, c.k,
-        c.H, c.cap, c.fp8 ? 1 : 0);
+        c.H, c.cap, c.fp8 ? 1 : 0, c.y_f32 ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -61,6 +61,7 @@ static_assert(kChunk % EP_DISPATCH_TPC == 0 && kChunk % EP_DISPATCH_REG_TPC == 0
 
 struct DispatchParams {
     const uint4 *x;
+    const float *scales_in;   // pre-quantised block scales [W][T][nb], or null
     const float *w;
     const int32_t *idx;
     const uint32_t *masks;
@@ -72,6 +73,7 @@ struct DispatchParams {
     uint32_t *words;
     uint32_t *dflags;
     int W, k, T, H, nch, cap, nvec, nb;
+    int row_bytes;            // payload bytes per row on both sides (bulk path)
     int notify;
     uint32_t epoch;
     int64_t timeout_ns;
@@ -120,7 +122,8 @@ __device__ __forceinline__ void chunk_slots(const DispatchParams &p, int g, int 
 }
 
 // Per-destination metadata of one token, written by one warp: all k
-// weights, all k expert ids, src_pos.
+// weights, all k expert ids, src_pos, and for a pre-quantised input its
+// block-scale row.
 __device__ __forceinline__ void token_metadata(const DispatchParams &p, int s, int t,
                                                uint32_t m, const int32_t *slots) {
     const int lane = threadIdx.x & 31;
@@ -142,6 +145,10 @@ __device__ __forceinline__ void token_metadata(const DispatchParams &p, int s, i
         }
         if (lane == 0)
             reinterpret_cast<int32_t *>(seg + p.off_src)[slot] = (int32_t)(s * p.T + t);
+        if (p.scales_in) {
+            float *dst = reinterpret_cast<float *>(seg + p.off_scales) + (int64_t)slot * p.nb;
+            for (int b = lane; b < p.nb; b += 32) dst[b] = __ldg(p.scales_in + tok * p.nb + b);
+        }
     }
 }
 
@@ -304,7 +311,9 @@ dispatch_kernel(const DispatchParams p) {
 }
 
 // ---------------------------------------------------------------- bulk path
-// bf16 rows by the Tensor Memory Accelerator's bulk copies: thread 0 runs a
+// Rows copied unchanged (bf16, or pre-quantised E4M3 codes whose scale rows
+// the metadata warps copy) by the Tensor Memory Accelerator's bulk copies:
+// thread 0 runs a
 // ring of STAGES row buffers in shared memory.  Each source row is brought
 // in ONCE by cp.async.bulk (completion counted on an mbarrier), then one
 // bulk store per destination writes it out; a stage is refilled once the
@@ -416,7 +425,7 @@ dispatch_bulk_kernel(const DispatchParams p) {
 
     if (warp == 0) {
         if (lane == 0) {
-            const uint32_t bytes = (uint32_t)p.nvec * 16u;
+            const uint32_t bytes = (uint32_t)p.row_bytes;
             const uint64_t pol = l2_evict_first_policy();
             auto issue = [&](int j) {
                 const int st = j % STAGES;
@@ -514,7 +523,7 @@ cudaError_t launch_dispatch_bulk(const Config &c, const DispatchParams &p,
                                  cudaStream_t st) {
     static size_t configured = 0;       // per instantiation
     static long share = -1;             // smem per CTA at the capped residency
-    const size_t row = (size_t)c.nvec * 16;
+    const size_t row = (size_t)p.row_bytes;
     size_t dyn = (size_t)STAGES * row;
     const size_t per_cta = (size_t)TPC * (size_t)(c.W < c.k ? c.W : c.k) * row;
     if (EP_DISPATCH_BULK_CTAS_PER_SM > 0 && per_cta >= 64 * 1024) {
@@ -551,6 +560,7 @@ cudaError_t launch_dispatch(const Config &c, const Workspace &ws,
                             const DispatchArgs &a, cudaStream_t st) {
     DispatchParams p;
     p.x = reinterpret_cast<const uint4 *>(a.x);
+    p.scales_in = a.scales_in;
     p.w = a.w;
     p.idx = a.idx;
     p.masks = ws.masks;
@@ -568,16 +578,20 @@ cudaError_t launch_dispatch(const Config &c, const Workspace &ws,
     p.dflags = ws.dflags;
     p.W = c.W; p.k = c.k; p.T = c.T; p.H = c.H; p.nch = c.nch; p.cap = c.cap;
     p.nvec = c.nvec; p.nb = c.nb;
+    p.row_bytes = c.fp8 ? c.H : c.H * 2;
     p.notify = c.early_notify ? 1 : 0;
     p.epoch = a.epoch;
     p.timeout_ns = c.timeout_ns;
     p.nt = a.nt;
-    if (c.fp8)
+    if (c.fp8 && !a.scales_in)      // fused quantisation
         return launch_dispatch_t<true, EP_DISPATCH_FP8_UNROLL, EP_DISPATCH_REG_TPC>(c, p, st);
+    // rows copied unchanged: bf16, or pre-quantised codes (H <= 16384 bytes)
 #if EP_DISPATCH_BULK_STAGES > 0
-    if ((size_t)kBulkStages * c.nvec * 16 <= 160 * 1024)
+    if ((size_t)kBulkStages * p.row_bytes <= 160 * 1024)
         return launch_dispatch_bulk<kBulkStages, EP_DISPATCH_TPC>(c, p, st);
 #endif
+    if (c.fp8)   // the register path copies bf16-sized vectors: not for codes
+        return cudaErrorInvalidValue;
     return launch_dispatch_t<false, EP_DISPATCH_UNROLL, EP_DISPATCH_REG_TPC>(c, p, st);
 }
 

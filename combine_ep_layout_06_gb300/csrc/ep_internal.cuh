@@ -44,6 +44,7 @@ struct Workspace {
 struct Config {
     int W, E, Er, k, H, T, cap;
     bool fp8;
+    bool y_f32;  // combine reads fp32 expert rows (else bf16)
     int nch;     // chunks per source rank = ceil(T / kChunk)
     int G;       // W * nch
     int Q;       // layout groups = ceil(G / kGroup)
@@ -70,7 +71,8 @@ cudaError_t launch_layout(const Config &c, const Workspace &ws,
                           cudaStream_t st, bool publish);
 
 struct DispatchArgs {
-    const void *x;         // [W][T][H] bf16
+    const void *x;         // [W][T][H] bf16, or E4M3 codes with scales_in
+    const float *scales_in;  // [W][T][H/128] pre-quantised block scales, or null
     const float *w;        // [W][T][k]
     const int32_t *idx;    // [W][T][k]
     TokenCounts nt;

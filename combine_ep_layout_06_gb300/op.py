@@ -31,16 +31,21 @@ class EpDispatchCombineConfig:
     early_notify: bool = False
     fused_recv: bool = False
     wait_timeout_ns: int = 0                 # 0 -> 1 s
+    combine_dtype: str = "bf16"              # expert rows combine reads: "bf16" | "fp32"
 
     def to_c(self) -> _lib.EpConfigC:
         dt = {"bf16": _lib.EP_DT_BF16, "fp8_e4m3": _lib.EP_DT_FP8_E4M3}
+        ct = {"bf16": _lib.EP_DT_BF16, "fp32": _lib.EP_DT_FP32}
         if self.dispatch_dtype not in dt:
             raise ValueError(f"dispatch_dtype {self.dispatch_dtype!r}")
+        if self.combine_dtype not in ct:
+            raise ValueError(f"combine_dtype {self.combine_dtype!r}")
         return _lib.EpConfigC(
             self.world_size, self.num_experts, self.topk, self.hidden,
             self.max_tokens_per_rank, self.max_recv_tokens_per_rank,
             dt[self.dispatch_dtype], int(self.early_notify),
-            int(self.fused_recv), 0, int(self.wait_timeout_ns))
+            int(self.fused_recv), ct[self.combine_dtype],
+            int(self.wait_timeout_ns))
 
 
 def workspace_size(cfg: EpDispatchCombineConfig) -> int:
@@ -116,11 +121,15 @@ class EpDispatchCombineOp:
         self.combine_flags = view(o.combine_flags, torch.int32, (W, W), (W, 1))
         p = ctypes.c_void_p()
         s = ctypes.c_int64()
-        check(self.L.ep_get_combine_input_buffer(self.h, _lib.EP_DT_BF16,
-                                                 ctypes.byref(p), ctypes.byref(s)),
+        y32 = c.combine_dtype == "fp32"
+        check(self.L.ep_get_combine_input_buffer(
+                  self.h, _lib.EP_DT_FP32 if y32 else _lib.EP_DT_BF16,
+                  ctypes.byref(p), ctypes.byref(s)),
               "ep_get_combine_input_buffer")
-        self.combine_input = view(p.value, torch.bfloat16, (W, cap, H),
-                                  (s.value // 2, H, 1))
+        self.y_dtype = torch.float32 if y32 else torch.bfloat16
+        esz = 4 if y32 else 2
+        self.combine_input = view(p.value, self.y_dtype, (W, cap, H),
+                                  (s.value // esz, H, 1))
         self.rank_stride_bytes = rs
 
     def epochs(self):
@@ -137,10 +146,19 @@ class EpDispatchCombineOp:
         arr = (ctypes.c_int32 * c.world_size)(*[int(n) for n in num_tokens])
         return arr
 
-    def _check_inputs(self, x, w, idx):
+    def _check_inputs(self, x, w, idx, scales=None):
         c = self.config
         W, T, H, k = c.world_size, c.max_tokens_per_rank, c.hidden, c.topk
-        if x.dtype != torch.bfloat16 or tuple(x.shape) != (W, T, H) or not x.is_contiguous():
+        if scales is not None:
+            # pre-quantised input: E4M3 codes (uint8 or float8_e4m3fn) + scales
+            if c.dispatch_dtype != "fp8_e4m3":
+                raise ValueError("scales (pre-quantised input) need an fp8_e4m3 dispatch")
+            if x.element_size() != 1 or tuple(x.shape) != (W, T, H) or not x.is_contiguous():
+                raise ValueError(f"pre-quantised input must be contiguous 1-byte [{W},{T},{H}]")
+            if scales.dtype != torch.float32 or tuple(scales.shape) != (W, T, H // 128) \
+                    or not scales.is_contiguous() or scales.device != self.device:
+                raise ValueError(f"scales must be contiguous fp32 [{W},{T},{H // 128}]")
+        elif x.dtype != torch.bfloat16 or tuple(x.shape) != (W, T, H) or not x.is_contiguous():
             raise ValueError(f"input must be contiguous bf16 [{W},{T},{H}]")
         if w.dtype != torch.float32 or tuple(w.shape) != (W, T, k) or not w.is_contiguous():
             raise ValueError(f"weights must be contiguous fp32 [{W},{T},{k}]")
@@ -165,7 +183,7 @@ class EpDispatchCombineOp:
         indices, recv_count): per-rank views [W][cap][...] into the receive
         segments (valid until the next dispatch / reset) and recv_count [W].
         Rows p >= recv_count[r] of rank r are unspecified."""
-        self._check_inputs(input, weights, indices)
+        self._check_inputs(input, weights, indices, scales)
         check(self.L.ep_dispatch(self.h, _ptr(input), _ptr(weights),
                                  _ptr(scales), _ptr(indices),
                                  self._counts(num_tokens), _stream(stream)),
@@ -174,18 +192,18 @@ class EpDispatchCombineOp:
 
     def dispatch_send(self, input, weights, scales=None, indices=None,
                       num_tokens=None, stream=None):
-        self._check_inputs(input, weights, indices)
+        self._check_inputs(input, weights, indices, scales)
         check(self.L.ep_dispatch_send(self.h, _ptr(input), _ptr(weights),
                                       _ptr(scales), _ptr(indices),
                                       self._counts(num_tokens), _stream(stream)),
               "ep_dispatch_send")
 
     def dispatch_send_replay(self, input, weights, indices, num_tokens=None,
-                             stream=None):
+                             stream=None, scales=None):
         """Routing replay: copy with the cached layout of the last call."""
-        self._check_inputs(input, weights, indices)
+        self._check_inputs(input, weights, indices, scales)
         check(self.L.ep_dispatch_send_replay(self.h, _ptr(input), _ptr(weights),
-                                             _ptr(indices),
+                                             _ptr(scales), _ptr(indices),
                                              self._counts(num_tokens),
                                              _stream(stream)),
               "ep_dispatch_send_replay")
@@ -205,11 +223,12 @@ class EpDispatchCombineOp:
                                       device=self.device)
         ys = 0
         if input is not None:
-            if input.dtype != torch.bfloat16 or input.dim() != 3 or \
+            if input.dtype != self.y_dtype or input.dim() != 3 or \
                     input.shape[0] != W or input.shape[2] != H or input.stride(2) != 1 \
                     or input.stride(1) != H:
-                raise ValueError("combine input must be bf16 [W][>=cap][H] with dense rows")
-            ys = input.stride(0) * 2
+                raise ValueError(f"combine input must be {self.y_dtype} [W][>=cap][H] "
+                                 "with dense rows")
+            ys = input.stride(0) * input.element_size()
         ws = 0
         if weights is not None:
             if weights.dtype != torch.float32 or weights.dim() != 3 or \
@@ -244,8 +263,8 @@ class EpDispatchCombineOp:
         """Source position s*T + t of every received row, int32 [W][cap]."""
         return self.src_pos
 
-    def get_registered_combine_input_buffer(self, dtype=torch.bfloat16):
-        if dtype != torch.bfloat16:
+    def get_registered_combine_input_buffer(self, dtype=None):
+        if dtype is not None and dtype != self.y_dtype:
             raise EpError(4, "get_registered_combine_input_buffer")
         return self.combine_input
 
@@ -259,7 +278,7 @@ class EpDispatchCombineOp:
 
     def identity_expert(self, y=None, stream=None):
         """Test harness: y_r = rows scaled by their rank-local weight sum."""
-        ys = 0 if y is None else y.stride(0) * 2
+        ys = 0 if y is None else y.stride(0) * y.element_size()
         check(self.L.ep_test_identity_expert(self.h, _ptr(y), ys, _stream(stream)),
               "ep_test_identity_expert")
         return self.combine_input if y is None else y

@@ -119,7 +119,9 @@ typedef struct {
                                          gather kernel does the receive wait
                                          itself, one warp per CTA, then a CTA
                                          barrier releases the gather warps */
-    int32_t reserved0;
+    int32_t combine_dtype;            /* element type of the expert rows that
+                                         combine reads: EP_DT_BF16 (0) or
+                                         EP_DT_FP32; the output is bf16 */
     int64_t wait_timeout_ns;          /* bound of every device wait; 0 = 1 s */
 } ep_config_t;
 
@@ -173,10 +175,15 @@ ep_status_t ep_layout(ep_handle_t *h, const int32_t *d_idx,
 
 /* Send phase of dispatch: layout, then the copy of every token row to each
  * of its destination ranks (with its k weights, k ids and src_pos), then
- * (early_notify) the ready flags.  d_x: [W][T][H] bf16, 16-byte aligned;
- * d_w: [W][T][k] fp32; d_scales: must be NULL (pre-quantised payloads are
- * not accepted); d_idx: [W][T][k] int32.  Inputs must stay unchanged until
- * the receive phase has been enqueued. */
+ * (early_notify) the ready flags.  d_w: [W][T][k] fp32; d_idx: [W][T][k]
+ * int32.  d_x and d_scales, 16-byte aligned:
+ *  - d_scales == NULL: d_x is [W][T][H] bf16; with an FP8 dispatch_dtype
+ *    every row is quantised on the way (fused per-128-element E4M3);
+ *  - d_scales != NULL (FP8 dispatch_dtype only; the pages' dispatch takes
+ *    `scales` beside `input` and "can carry already-quantized FP8
+ *    payloads"): d_x is [W][T][H] E4M3 codes and d_scales [W][T][H/128]
+ *    fp32 block scales, both copied unchanged.
+ * Inputs must stay unchanged until the receive phase has been enqueued. */
 ep_status_t ep_dispatch_send(ep_handle_t *h, const void *d_x, const float *d_w,
                              const float *d_scales, const int32_t *d_idx,
                              const int32_t *h_num_tokens, void *stream);
@@ -194,17 +201,19 @@ ep_status_t ep_dispatch(ep_handle_t *h, const void *d_x, const float *d_w,
 
 /* Routing replay: the copy (and notify) of ep_dispatch_send, reusing the
  * layout of the last ep_layout / ep_dispatch_send call for the same indices
- * and token counts, without recomputing it.  h_num_tokens must equal the
- * layout's.  BAD_STATE without a layout. */
+ * and token counts, without recomputing it.  d_x / d_scales as in
+ * ep_dispatch_send; h_num_tokens must equal the layout's.  BAD_STATE
+ * without a layout. */
 ep_status_t ep_dispatch_send_replay(ep_handle_t *h, const void *d_x,
-                                    const float *d_w, const int32_t *d_idx,
+                                    const float *d_w, const float *d_scales,
+                                    const int32_t *d_idx,
                                     const int32_t *h_num_tokens, void *stream);
 
 ep_status_t ep_dispatch_outputs(const ep_handle_t *h, ep_dispatch_out_t *out);
 
 /* The pre-registered combine input buffer of rank 0 (the expert writes
  * y_r rows here; rank r's rows start at *d_ptr + r * *rank_stride_bytes).
- * Only EP_DT_BF16 is provided. */
+ * dtype must be the config's combine_dtype (else EP_ERR_NOT_FOUND). */
 ep_status_t ep_get_combine_input_buffer(const ep_handle_t *h, int32_t dtype,
                                         void **d_ptr,
                                         int64_t *rank_stride_bytes);
@@ -215,7 +224,7 @@ ep_status_t ep_combine_send(ep_handle_t *h, void *stream);
 
 /* Receive phase of combine (source side): wait for the combine send, then
  * gather-reduce.  d_y: NULL for the registered buffer, else rank r's rows at
- * d_y + r*y_rank_stride_bytes ([cap][H] bf16, 16-byte aligned rows).
+ * d_y + r*y_rank_stride_bytes ([cap][H] of combine_dtype, 16-byte aligned).
  * d_w_in: NULL, or rank r's expert-side weight rows [cap][k] fp32 at
  * d_w_in + r*w_rank_stride_bytes.  d_idx: NULL, or the [W][T][k] ids of the
  * dispatch (checked: a token whose destination set differs sets the
@@ -247,8 +256,9 @@ ep_status_t ep_get_error(ep_handle_t *h, uint32_t *mask, void *stream);
  * benchmark's correctness check ("Validation before tuning").  For each
  * received row p < min(recv_count[r], cap) of every rank r:
  * alpha = ordered fp32 sum of the row's weights whose expert lives on r,
- * y_r[p][h] = bf16_rne(fl32(v_h * alpha)), v = the bf16 payload, or
- * fl32(e4m3_value(q) * scale) for FP8.  d_y as in ep_combine_recv. */
+ * y_r[p][h] = bf16_rne(fl32(v_h * alpha)) (fp32 rows: fl32(v_h * alpha)),
+ * v = the bf16 payload, or fl32(e4m3_value(q) * scale) for FP8.  d_y as in
+ * ep_combine_recv. */
 ep_status_t ep_test_identity_expert(ep_handle_t *h, void *d_y,
                                     int64_t y_rank_stride_bytes, void *stream);
 

@@ -47,7 +47,7 @@ def test_status_strings(L):
 def _cfg(**kw):
     base = dict(world_size=8, num_experts=256, topk=8, hidden=7168,
                 max_tokens_per_rank=4096, max_recv_tokens_per_rank=0,
-                dispatch_dtype=0, early_notify=0, fused_recv=0, reserved0=0,
+                dispatch_dtype=0, early_notify=0, fused_recv=0, combine_dtype=0,
                 wait_timeout_ns=0)
     base.update(kw)
     return _lib.EpConfigC(**base)
@@ -74,10 +74,13 @@ def test_workspace_size_and_config_validation(L):
            dict(topk=0), dict(topk=33), dict(hidden=7170), dict(hidden=0),
            dict(max_tokens_per_rank=0), dict(dispatch_dtype=1, hidden=7168 + 8),
            dict(dispatch_dtype=7), dict(max_recv_tokens_per_rank=-1),
-           dict(fused_recv=1, early_notify=0)]
+           dict(fused_recv=1, early_notify=0), dict(combine_dtype=1),
+           dict(combine_dtype=5)]
     for b in bad:
         assert _size(L, **b)[0] == 3, b      # EP_ERR_INVALID_ARGS
     assert _size(L, max_recv_tokens_per_rank=100)[1] < n
+    st32, n32 = _size(L, combine_dtype=2)         # fp32 combine rows
+    assert st32 == 0 and n32 > n
 
 
 def test_create_rejects_bad_workspace_without_touching_the_gpu(L):
