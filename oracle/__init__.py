@@ -82,6 +82,10 @@ def _declare(L):
         "or_identity_expert_f32": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
                                         _P, _P]),
         "or_combine_f32": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+        "or_expert_layout": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P]),
+        "or_group_rows": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P,
+                               _P, _P, _P, _P]),
+        "or_ungroup": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
         "or_combine": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
         "or_combine_tokens": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _I,
                                    _P, _P]),
@@ -333,6 +337,46 @@ def combine_f32(wl, num_tokens, pos, y, w_in, cap):
                          _p(None if w_in is None else _c(w_in, np.float32)),
                          _p(out), _p(out_w))
     return out, out_w
+
+
+def expert_layout(wl, recv_count, out_idx, cap):
+    """Standard-MoE grouping layout: (count [W][Er], offset [W][Er],
+    entry_slot [W][cap][k])."""
+    W, k, Er = wl.world_size, wl.topk, wl.experts_per_rank
+    count = np.zeros((W, Er), np.int32)
+    offset = np.zeros((W, Er), np.int32)
+    slot = np.zeros((W, cap, k), np.int32)
+    lib().or_expert_layout(W, wl.num_experts, k, cap, _p(_c(recv_count, np.int32)),
+                           _p(_c(out_idx, np.int32)), _p(count), _p(offset), _p(slot))
+    return count, offset, slot
+
+
+def group_rows(wl, recv_count, out, out_scales, out_w, entry_slot, cap, gcap):
+    """Grouped copy: (xg [W][gcap][H], xg_scales [W][gcap][nb], g_src, g_w);
+    slots never written stay zero."""
+    W, H, k = wl.world_size, wl.hidden, wl.topk
+    fp8 = out.dtype == np.uint8
+    nb = H // 128 if fp8 else 0
+    xg = np.zeros((W, gcap, H), out.dtype)
+    xs = np.zeros((W, gcap, max(nb, 1)), np.float32)
+    src = np.zeros((W, gcap), np.int32)
+    gw = np.zeros((W, gcap), np.float32)
+    osc = _c(out_scales, np.float32) if fp8 else np.zeros((W, cap, 1), np.float32)
+    lib().or_group_rows(W, k, H, 1 if fp8 else 2, nb, cap, gcap,
+                        _p(_c(recv_count, np.int32)), _p(_c(out, out.dtype)), _p(osc),
+                        _p(_c(out_w, np.float32)), _p(_c(entry_slot, np.int32)),
+                        _p(xg), _p(xs), _p(src), _p(gw))
+    return xg, xs[..., :nb], src, gw
+
+
+def ungroup(wl, recv_count, out_w, entry_slot, yg, cap, gcap):
+    """Weighted per-row sum of the grouped expert outputs: y [W][cap][H]."""
+    W, H, k = wl.world_size, wl.hidden, wl.topk
+    y = np.zeros((W, cap, H), np.uint16)
+    lib().or_ungroup(W, k, H, cap, gcap, _p(_c(recv_count, np.int32)),
+                     _p(_c(out_w, np.float32)), _p(_c(entry_slot, np.int32)),
+                     _p(_c(yg, np.uint16)), _p(y))
+    return y
 
 
 def run_all(inp, cap=None):

@@ -572,3 +572,106 @@ int or_combine_f32(int W, int k, int T, int H, int cap, const int32_t *num_token
         }
     return OR_OK;
 }
+
+/* ------------------------------------------- standard-MoE conversion */
+
+/* Standard-MoE grouping of one rank's received rows (the EPv2 feature list
+ * of "Choosing an EP API and backend" names a "standard-MoE conversion";
+ * reading: per-local-expert contiguous groups).  On rank r, with
+ * n_r = min(recv_count[r], cap) received rows, the entries are the pairs
+ * (p, j), p < n_r, j < k, whose expert out_idx[r][p][j] lives on r, in
+ * (p, j) ascending order; e = out_idx - r*Er is the entry's local expert.
+ *   count[r][e]  = number of entries of expert e
+ *   offset[r][e] = sum_{e' < e} count[r][e']
+ *   slot(p, j)   = offset[r][e] + #{entries of e before (p, j)}
+ * entry_slot[r][p][j] = slot(p, j), or -1 for a non-local j or p >= n_r.
+ * count, offset int32 [W][Er]; entry_slot int32 [W][cap][k]. */
+int or_expert_layout(int W, int E, int k, int cap, const int32_t *recv_count,
+                     const int32_t *out_idx, int32_t *count, int32_t *offset,
+                     int32_t *entry_slot)
+{
+    int Er = E / W;
+    for (int r = 0; r < W; ++r) {
+        int n = recv_count[r] < cap ? recv_count[r] : cap;
+        for (int e = 0; e < Er; ++e) count[r * Er + e] = 0;
+        for (int p = 0; p < n; ++p)
+            for (int j = 0; j < k; ++j) {
+                int32_t g = out_idx[((int64_t)r * cap + p) * k + j];
+                if (g / Er == r) count[r * Er + (g - r * Er)] += 1;
+            }
+        int32_t run = 0;
+        for (int e = 0; e < Er; ++e) { offset[r * Er + e] = run; run += count[r * Er + e]; }
+        for (int64_t o = (int64_t)r * cap * k; o < (int64_t)(r + 1) * cap * k; ++o)
+            entry_slot[o] = -1;
+        for (int e = 0; e < Er; ++e) {
+            int32_t before = 0;   /* entries of e seen so far, in (p, j) order */
+            for (int p = 0; p < n; ++p)
+                for (int j = 0; j < k; ++j) {
+                    int64_t o = ((int64_t)r * cap + p) * k + j;
+                    int32_t g = out_idx[o];
+                    if (g / Er == r && g - r * Er == e) {
+                        entry_slot[o] = offset[r * Er + e] + before;
+                        before += 1;
+                    }
+                }
+        }
+    }
+    return OR_OK;
+}
+
+/* Grouped copy: for every entry (p, j) of rank r with q = entry_slot < gcap,
+ *   xg[r][q] = out[r][p] (payload row, elem_bytes per element),
+ *   xg_scales[r][q] = out_scales[r][p] (FP8 only, nb floats),
+ *   g_src[r][q] = p*k + j,  g_w[r][q] = out_w[r][p][j].
+ * Payload rows are H*elem_bytes bytes. */
+int or_group_rows(int W, int k, int H, int elem_bytes, int nb, int cap, int gcap,
+                  const int32_t *recv_count, const void *out, const float *out_scales,
+                  const float *out_w, const int32_t *entry_slot, void *xg,
+                  float *xg_scales, int32_t *g_src, float *g_w)
+{
+    int64_t rb = (int64_t)H * elem_bytes;
+    for (int r = 0; r < W; ++r) {
+        int n = recv_count[r] < cap ? recv_count[r] : cap;
+        for (int p = 0; p < n; ++p)
+            for (int j = 0; j < k; ++j) {
+                int64_t o = ((int64_t)r * cap + p) * k + j;
+                int32_t q = entry_slot[o];
+                if (q < 0 || q >= gcap) continue;
+                int64_t rq = (int64_t)r * gcap + q;
+                memcpy((char *)xg + rq * rb, (const char *)out + ((int64_t)r * cap + p) * rb, rb);
+                for (int b = 0; b < nb; ++b)
+                    xg_scales[rq * nb + b] = out_scales[((int64_t)r * cap + p) * nb + b];
+                g_src[rq] = p * k + j;
+                g_w[rq] = out_w[o];
+            }
+    }
+    return OR_OK;
+}
+
+/* Un-grouping (the standard MoE's weighted sum of a token's expert outputs
+ * on one rank): for each received row p < min(recv_count[r], cap),
+ *   acc = +0.0f; for j ascending with q = entry_slot[r][p][j] in [0, gcap):
+ *     acc = fl32(acc + fl32(out_w[r][p][j] * fp32(yg[r][q][h])))
+ *   y[r][p][h] = bf16_rne(acc).
+ * yg uint16 [W][gcap][H]; y uint16 [W][cap][H]. */
+int or_ungroup(int W, int k, int H, int cap, int gcap, const int32_t *recv_count,
+               const float *out_w, const int32_t *entry_slot, const uint16_t *yg,
+               uint16_t *y)
+{
+    for (int r = 0; r < W; ++r) {
+        int n = recv_count[r] < cap ? recv_count[r] : cap;
+        for (int p = 0; p < n; ++p)
+            for (int h = 0; h < H; ++h) {
+                float acc = 0.0f;
+                for (int j = 0; j < k; ++j) {
+                    int64_t o = ((int64_t)r * cap + p) * k + j;
+                    int32_t q = entry_slot[o];
+                    if (q < 0 || q >= gcap) continue;
+                    float prod = out_w[o] * or_bf16_to_f32(yg[((int64_t)r * gcap + q) * H + h]);
+                    acc = acc + prod;
+                }
+                y[((int64_t)r * cap + p) * H + h] = or_bf16_rne(acc);
+            }
+    }
+    return OR_OK;
+}

@@ -175,3 +175,28 @@ def combine_f32(disp, ys, W, T, H, num_tokens):
                 acc = (acc + ys[r][i]).astype(np.float32)
             out[(s, t)] = torch_bf16_bits(acc)
     return out
+
+
+def expert_groups(out_idx_rows, r, Er):
+    """Entries of rank r as a dict e -> sorted list of (p, j), by listing
+    every local selection and sorting by (expert, p, j)."""
+    ent = []
+    for p, ids in enumerate(out_idx_rows):
+        for j, g in enumerate(ids):
+            if int(g) // Er == r:
+                ent.append((int(g) - r * Er, p, j))
+    groups = {}
+    for e, p, j in sorted(ent):
+        groups.setdefault(e, []).append((p, j))
+    return groups
+
+
+def ungroup_row(w_row, ys):
+    """bf16(sum over the row's entries, j ascending, of f32(w_j * y_j))."""
+    acc = None
+    for w, y in ys:
+        prod = (np.float32(w) * to_f32(y)).astype(np.float32)
+        if acc is None:
+            acc = np.zeros_like(prod)
+        acc = (acc + prod).astype(np.float32)
+    return None if acc is None else torch_bf16_bits(acc)

@@ -551,3 +551,65 @@ def test_fp32_combine_order_is_ascending_rank():
     y[2, 0] = -1.0
     out, _ = oracle.combine_f32(wl, nt, pos, y, None, W)
     assert np.all(out[0, 0] == 0)
+
+
+# ------------------------------------------------- standard-MoE conversion
+
+@pytest.mark.parametrize("seed,fp8,dup", [(0, False, False), (1, False, True),
+                                          (2, True, False), (3, False, True)])
+def test_expert_grouping_matches_bruteforce(seed, fp8, dup):
+    rng = np.random.default_rng(900 + seed)
+    wl, inp = _random_case(rng, 3, 4, 3, 13, 256 if fp8 else 32, dup=dup, fp8=fp8)
+    res = oracle.run_all(inp)
+    cap = res["cap"]
+    W, Er, k = wl.world_size, wl.experts_per_rank, wl.topk
+    count, offset, slot = oracle.expert_layout(wl, res["recv_count"], res["out_idx"], cap)
+    gcap = cap * k
+    xg, xs, src, gw = oracle.group_rows(wl, res["recv_count"], res["out"],
+                                        res["out_scales"], res["out_w"], slot, cap, gcap)
+    for r in range(W):
+        n = res["recv_count"][r]
+        groups = bf.expert_groups(res["out_idx"][r, :n], r, Er)
+        q = 0
+        for e in range(Er):
+            ent = groups.get(e, [])
+            assert count[r, e] == len(ent) and offset[r, e] == q
+            for (p, j) in ent:
+                assert slot[r, p, j] == q
+                assert np.array_equal(xg[r, q], res["out"][r, p])
+                if fp8:
+                    assert np.array_equal(xs[r, q], res["out_scales"][r, p])
+                assert src[r, q] == p * k + j and gw[r, q] == res["out_w"][r, p, j]
+                q += 1
+        assert count[r].sum() == sum(len(v) for v in groups.values())
+        nonlocal_ = (res["out_idx"][r, :n] // Er) != r
+        assert np.all(slot[r, :n][nonlocal_] == -1) and np.all(slot[r, n:] == -1)
+    # un-grouping with arbitrary expert outputs: weighted ordered sums
+    yg = bf.torch_bf16_bits(rng.standard_normal((W, gcap, wl.hidden)).astype(np.float32))
+    y = oracle.ungroup(wl, res["recv_count"], res["out_w"], slot, yg, cap, gcap)
+    for r in range(W):
+        for p in range(res["recv_count"][r]):
+            pairs = [(res["out_w"][r, p, j], yg[r, slot[r, p, j]]) for j in range(k)
+                     if slot[r, p, j] >= 0]
+            exp = bf.ungroup_row(None, pairs)
+            assert np.array_equal(y[r, p], exp)
+
+
+def test_grouped_identity_experts_give_back_the_input():
+    """Identity experts per entry (yg = xg) un-grouped and combined return x
+    within the rounding of the weighted sums."""
+    wl = _reduced("dsv3").scaled(48, hidden=128)
+    inp = gen.make_inputs(wl)
+    res = oracle.run_all(inp)
+    cap = res["cap"]
+    count, offset, slot = oracle.expert_layout(wl, res["recv_count"], res["out_idx"], cap)
+    gcap = cap * wl.topk
+    xg, _, _, _ = oracle.group_rows(wl, res["recv_count"], res["out"], None,
+                                    res["out_w"], slot, cap, gcap)
+    y = oracle.ungroup(wl, res["recv_count"], res["out_w"], slot, xg, cap, gcap)
+    out, _ = oracle.combine(wl, inp.num_tokens, res["pos"], y, None, cap)
+    x = bf.to_f32(inp.x_bits)
+    got = bf.to_f32(out)
+    assert np.all(np.abs(got - x) <= np.abs(x) * 2.0 ** -8 * 12)
+    # every token's k selections land in exactly one group slot each
+    assert count.sum() == wl.world_size * wl.max_tokens_per_rank * wl.topk
