@@ -59,6 +59,9 @@ def parse():
                     help="FP8 workloads: dispatch a pre-quantised payload (codes + scales)")
     ap.add_argument("--combine-dtype", choices=["bf16", "fp32"], default="bf16",
                     help="element type of the expert rows combine reads")
+    ap.add_argument("--moe-group", type=int, default=0, metavar="GCAP",
+                    help="also time the standard-MoE grouping / un-grouping with "
+                         "GCAP grouped rows per rank (reported beside the step)")
     return ap.parse_args()
 
 
@@ -211,7 +214,8 @@ def run_ours(args, rank, world, local_rank):
     cfg = EpDispatchCombineConfig(W, wl.num_experts, k, H, T,
                                   max_recv_tokens_per_rank=args.cap,
                                   dispatch_dtype="fp8_e4m3" if wl.fp8 else "bf16",
-                                  combine_dtype=args.combine_dtype)
+                                  combine_dtype=args.combine_dtype,
+                                  max_grouped_rows_per_rank=args.moe_group)
     op = EpDispatchCombineOp(cfg, device=dev)
     x = torch.from_numpy(inp.x_bits.view(np.int16)).to(dev).view(torch.bfloat16)
     xsc = None
@@ -360,6 +364,38 @@ def run_ours(args, rank, world, local_rank):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e_ms}
 
+    moe = None
+    if args.moe_group:
+        # standard-MoE conversion after the step's dispatch: grouping, identity
+        # experts (a copy, untimed), un-grouping into the combine buffer
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        gms, ums = [], []
+        with torch.cuda.stream(stream):
+            for i in range(13):
+                ev[0].record(stream)
+                op.moe_group(stream=stream)
+                ev[1].record(stream)
+                op.moe_y.copy_(op.moe_x)
+                ev[2].record(stream)
+                op.moe_ungroup(stream=stream)
+                ev[3].record(stream)
+                stream.synchronize()
+                if i >= 3:
+                    gms.append(ev[0].elapsed_time(ev[1]))
+                    ums.append(ev[2].elapsed_time(ev[3]))
+        st_m, mask_m = op.get_error(stream)
+        n_ent = int(op.moe_count.sum().item())
+        rowb = H * (1 if wl.fp8 else 2)
+        g_bytes = P * rowb + n_ent * (rowb + 8)
+        u_bytes = n_ent * (2 * H + 8) + P * 2 * H
+        g_ms, u_ms = float(np.median(gms)), float(np.median(ums))
+        moe = {"entries": n_ent, "gcap": args.moe_group, "errors": int(mask_m),
+               "group_ms": g_ms, "ungroup_ms": u_ms,
+               "group_gb_per_s": g_bytes / (g_ms / 1e3) / 1e9,
+               "ungroup_gb_per_s": u_bytes / (u_ms / 1e3) / 1e9,
+               "group_algorithmic_bytes": int(g_bytes),
+               "ungroup_algorithmic_bytes": int(u_bytes)}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, inp)
@@ -419,6 +455,8 @@ def run_ours(args, rank, world, local_rank):
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
+    if moe is not None:
+        res["standard_moe"] = moe
     return res
 
 

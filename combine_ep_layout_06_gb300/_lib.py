@@ -48,6 +48,24 @@ class EpConfigC(ctypes.Structure):
         ("fused_recv", ctypes.c_int32),
         ("combine_dtype", ctypes.c_int32),
         ("wait_timeout_ns", ctypes.c_int64),
+        ("max_grouped_rows_per_rank", ctypes.c_int32),
+        ("reserved1", ctypes.c_int32),
+    ]
+
+
+class EpMoeOutC(ctypes.Structure):
+    _fields_ = [
+        ("xg", ctypes.c_void_p),
+        ("xg_scales", ctypes.c_void_p),
+        ("g_src", ctypes.c_void_p),
+        ("g_w", ctypes.c_void_p),
+        ("yg", ctypes.c_void_p),
+        ("entry_slot", ctypes.c_void_p),
+        ("rank_stride_bytes", ctypes.c_int64),
+        ("count", ctypes.c_void_p),
+        ("offset", ctypes.c_void_p),
+        ("gcap", ctypes.c_int32),
+        ("experts_per_rank", ctypes.c_int32),
     ]
 
 
@@ -94,6 +112,9 @@ SIGNATURES = {
     "ep_reset": (_S, [_P, _P]),
     "ep_get_error": (_S, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
     "ep_test_identity_expert": (_S, [_P, _P, _I64, _P]),
+    "ep_moe_group": (_S, [_P, _P]),
+    "ep_moe_outputs": (_S, [_P, ctypes.POINTER(EpMoeOutC)]),
+    "ep_moe_ungroup": (_S, [_P, _P, _I64, _P]),
     "ep_layout_noalloc": (_S, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
 }
 

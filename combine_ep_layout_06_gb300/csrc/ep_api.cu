@@ -60,6 +60,11 @@ ep_status_t make_config(const ep_config_t *in, Config *c) {
     c->fused_recv = env_flag("EP_FUSED_RECV", in->fused_recv ? 1 : 0) != 0;
     if (c->fused_recv && !c->early_notify) return EP_ERR_INVALID_ARGS;
     c->timeout_ns = in->wait_timeout_ns > 0 ? in->wait_timeout_ns : 1000000000LL;
+    if (in->max_grouped_rows_per_rank < 0 ||
+        (int64_t)in->max_grouped_rows_per_rank > (int64_t)1 << 30)
+        return EP_ERR_INVALID_ARGS;
+    c->gcap = in->max_grouped_rows_per_rank;
+    c->nrc = (c->cap + kChunk - 1) / kChunk;
     return EP_SUCCESS;
 }
 
@@ -103,6 +108,12 @@ void plan_workspace(const Config &c, char *base, Workspace *ws) {
     ws->recv_count = reinterpret_cast<int32_t *>(take(W * 4));
     ws->masks = reinterpret_cast<uint32_t *>(take(W * T * 4));
     ws->pos = reinterpret_cast<int32_t *>(take(W * T * W * 4));
+    const size_t Er = c.Er, nrc = c.gcap ? c.nrc : 0;
+    const bool moe = c.gcap > 0;
+    ws->moe_cnt = reinterpret_cast<int32_t *>(take(W * nrc * Er * 4));
+    ws->moe_base = reinterpret_cast<int32_t *>(take(W * nrc * Er * 4));
+    ws->moe_count = reinterpret_cast<int32_t *>(take(moe ? W * Er * 4 : 0));
+    ws->moe_offset = reinterpret_cast<int32_t *>(take(moe ? W * Er * 4 : 0));
     // one rank segment
     const size_t cap = c.cap, H = c.H, k = c.k;
     size_t so = 0;
@@ -117,6 +128,13 @@ void plan_workspace(const Config &c, char *base, Workspace *ws) {
     ws->off_idx = seg_take(cap * k * 4);
     ws->off_src = seg_take(cap * 4);
     ws->off_comb = seg_take(cap * H * (c.y_f32 ? 4 : 2));
+    const size_t gc = c.gcap;
+    ws->off_xg = seg_take(gc * H * (c.fp8 ? 1 : 2));
+    ws->off_xgs = seg_take(c.fp8 ? gc * c.nb * 4 : 0);
+    ws->off_gsrc = seg_take(gc * 4);
+    ws->off_gw = seg_take(gc * 4);
+    ws->off_yg = seg_take(gc * H * 2);
+    ws->off_eslot = seg_take(moe ? cap * k * 4 : 0);
     ws->seg_stride = (int64_t)so;
     ws->seg0 = base ? base + off : nullptr;
     ws->total_bytes = off + so * W;
@@ -237,6 +255,7 @@ static ep_status_t dispatch_send_impl(ep_handle_t *h, const void *d_x,
                                       const TokenCounts &nt, bool run_layout,
                                       bool publish, cudaStream_t st) {
     if (h->cfg.early_notify) ++h->dispatch_epoch;
+    h->moe_valid = false;             // a grouping belongs to one dispatch
     if (run_layout) {
         const ep_status_t s =
             gpu(h, launch_layout(h->cfg, h->ws, d_idx, nt, st, publish), "layout");
@@ -459,6 +478,55 @@ ep_status_t ep_combine(ep_handle_t *h, const void *d_y, int64_t y_rank_stride_by
     return gpu(h, launch_combine(h->cfg, h->ws, a, st), "combine");
 }
 
+ep_status_t ep_moe_group(ep_handle_t *h, void *stream) {
+    if (!h) return EP_ERR_INVALID_ARGS;
+    if (h->cfg.gcap <= 0) return EP_ERR_INVALID_ARGS;
+    if (!h->layout_valid || h->dispatch_pending) return EP_ERR_BAD_STATE;
+    const ep_status_t s = gpu(h, launch_moe_group(h->cfg, h->ws, static_cast<cudaStream_t>(stream)),
+                              "moe_group");
+    if (s == EP_SUCCESS) h->moe_valid = true;
+    return s;
+}
+
+ep_status_t ep_moe_outputs(const ep_handle_t *h, ep_moe_out_t *o) {
+    if (!h || !o) return EP_ERR_INVALID_ARGS;
+    if (h->cfg.gcap <= 0) return EP_ERR_INVALID_ARGS;
+    const Workspace &ws = h->ws;
+    o->xg = ws.seg0 + ws.off_xg;
+    o->xg_scales = h->cfg.fp8 ? reinterpret_cast<float *>(ws.seg0 + ws.off_xgs) : nullptr;
+    o->g_src = reinterpret_cast<int32_t *>(ws.seg0 + ws.off_gsrc);
+    o->g_w = reinterpret_cast<float *>(ws.seg0 + ws.off_gw);
+    o->yg = ws.seg0 + ws.off_yg;
+    o->entry_slot = reinterpret_cast<int32_t *>(ws.seg0 + ws.off_eslot);
+    o->rank_stride_bytes = ws.seg_stride;
+    o->count = ws.moe_count;
+    o->offset = ws.moe_offset;
+    o->gcap = h->cfg.gcap;
+    o->experts_per_rank = h->cfg.Er;
+    return EP_SUCCESS;
+}
+
+ep_status_t ep_moe_ungroup(ep_handle_t *h, const void *d_yg, int64_t yg_stride,
+                           void *stream) {
+    if (!h) return EP_ERR_INVALID_ARGS;
+    const Config &c = h->cfg;
+    if (c.gcap <= 0 || c.y_f32) return EP_ERR_INVALID_ARGS;
+    const int64_t rows = (int64_t)c.gcap * c.H * 2;
+    const char *yg;
+    if (d_yg) {
+        if (yg_stride == 0) yg_stride = rows;
+        if (!aligned(d_yg, 16) || yg_stride % 16 != 0 || yg_stride < rows)
+            return EP_ERR_INVALID_ARGS;
+        yg = static_cast<const char *>(d_yg);
+    } else {
+        yg = h->ws.seg0 + h->ws.off_yg;
+        yg_stride = h->ws.seg_stride;
+    }
+    if (!h->moe_valid || !h->layout_valid) return EP_ERR_BAD_STATE;
+    return gpu(h, launch_moe_ungroup(c, h->ws, yg, yg_stride, static_cast<cudaStream_t>(stream)),
+               "moe_ungroup");
+}
+
 ep_status_t ep_reset(ep_handle_t *h, void *stream) {
     if (!h) return EP_ERR_INVALID_ARGS;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -474,6 +542,7 @@ ep_status_t ep_reset(ep_handle_t *h, void *stream) {
     h->layout_valid = false;
     h->dispatch_pending = false;
     h->combine_pending = false;
+    h->moe_valid = false;
     return EP_SUCCESS;
 }
 

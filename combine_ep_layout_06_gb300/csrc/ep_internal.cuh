@@ -20,6 +20,7 @@ constexpr int kGroup = 8;
 constexpr int kWordErr = 0;        // sticky device error word
 constexpr int kWordLayoutDone = 1; // "last CTA" ticket of the layout kernel
 constexpr int kWordSrcDone = 8;    // [W] per-source ticket of the dispatch copy
+constexpr int kWordMoeDone = 40;   // "last CTA" ticket of the grouping scan
 constexpr int kCounterWords = 64;  // 256 bytes
 
 struct Workspace {
@@ -34,10 +35,16 @@ struct Workspace {
     int32_t *recv_count;   // [W] published by the receive step
     uint32_t *masks;       // [W][T]   destination-rank bit mask per token
     int32_t *pos;          // [W][T][W]
+    // standard-MoE grouping (when gcap > 0)
+    int32_t *moe_cnt;      // [W][nrc][Er] entries per (rank, 32-row chunk, expert)
+    int32_t *moe_base;     // [W][nrc][Er] exclusive prefix over chunks
+    int32_t *moe_count;    // [W][Er]
+    int32_t *moe_offset;   // [W][Er]
     // rank-0 segment; rank r's copy is at + r * seg_stride bytes
     char *seg0;
     int64_t seg_stride;
     int64_t off_out, off_scales, off_w, off_idx, off_src, off_comb;
+    int64_t off_xg, off_xgs, off_gsrc, off_gw, off_yg, off_eslot;   // grouping
     size_t total_bytes;
 };
 
@@ -48,6 +55,8 @@ struct Config {
     int nch;     // chunks per source rank = ceil(T / kChunk)
     int G;       // W * nch
     int Q;       // layout groups = ceil(G / kGroup)
+    int gcap;    // grouped rows per rank (0: no standard-MoE grouping)
+    int nrc;     // 32-row chunks of received rows per rank = ceil(cap / 32)
     int nvec;    // 16-byte vectors per bf16 row = H / 8
     int nb;      // FP8 blocks per row = H / 128 (0 for bf16)
     bool early_notify, fused_recv;
@@ -106,6 +115,10 @@ struct CombineArgs {
 cudaError_t launch_combine(const Config &c, const Workspace &ws,
                            const CombineArgs &a, cudaStream_t st);
 
+cudaError_t launch_moe_group(const Config &c, const Workspace &ws, cudaStream_t st);
+cudaError_t launch_moe_ungroup(const Config &c, const Workspace &ws, const char *yg,
+                               int64_t yg_stride, cudaStream_t st);
+
 cudaError_t launch_identity_expert(const Config &c, const Workspace &ws,
                                    char *y, int64_t y_stride, cudaStream_t st);
 
@@ -123,6 +136,7 @@ struct ep_handle {
     bool layout_valid;      // a layout exists for combine / replay
     bool dispatch_pending;  // sent, not yet received
     bool combine_pending;   // combine sent, not yet received
+    bool moe_valid;         // a standard-MoE grouping exists for ungroup
     ep::TokenCounts layout_nt;
     int log_level;
 };

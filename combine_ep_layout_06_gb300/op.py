@@ -32,6 +32,7 @@ class EpDispatchCombineConfig:
     fused_recv: bool = False
     wait_timeout_ns: int = 0                 # 0 -> 1 s
     combine_dtype: str = "bf16"              # expert rows combine reads: "bf16" | "fp32"
+    max_grouped_rows_per_rank: int = 0       # standard-MoE grouping (0: off)
 
     def to_c(self) -> _lib.EpConfigC:
         dt = {"bf16": _lib.EP_DT_BF16, "fp8_e4m3": _lib.EP_DT_FP8_E4M3}
@@ -45,7 +46,7 @@ class EpDispatchCombineConfig:
             self.max_tokens_per_rank, self.max_recv_tokens_per_rank,
             dt[self.dispatch_dtype], int(self.early_notify),
             int(self.fused_recv), ct[self.combine_dtype],
-            int(self.wait_timeout_ns))
+            int(self.wait_timeout_ns), int(self.max_grouped_rows_per_rank), 0)
 
 
 def workspace_size(cfg: EpDispatchCombineConfig) -> int:
@@ -131,6 +132,20 @@ class EpDispatchCombineOp:
         self.combine_input = view(p.value, self.y_dtype, (W, cap, H),
                                   (s.value // esz, H, 1))
         self.rank_stride_bytes = rs
+        if c.max_grouped_rows_per_rank > 0:
+            m = _lib.EpMoeOutC()
+            check(self.L.ep_moe_outputs(self.h, ctypes.byref(m)), "ep_moe_outputs")
+            g, Er = m.gcap, m.experts_per_rank
+            self.moe_x = view(m.xg, torch.uint8 if fp8 else torch.bfloat16, (W, g, H),
+                              (rs // (1 if fp8 else 2), H, 1))
+            self.moe_x_scales = (view(m.xg_scales, torch.float32, (W, g, nb),
+                                      (rs // 4, nb, 1)) if fp8 else None)
+            self.moe_src = view(m.g_src, torch.int32, (W, g), (rs // 4, 1))
+            self.moe_w = view(m.g_w, torch.float32, (W, g), (rs // 4, 1))
+            self.moe_y = view(m.yg, torch.bfloat16, (W, g, H), (rs // 2, H, 1))
+            self.moe_entry_slot = view(m.entry_slot, torch.int32, (W, cap, k), (rs // 4, k, 1))
+            self.moe_count = view(m.count, torch.int32, (W, Er), (Er, 1))
+            self.moe_offset = view(m.offset, torch.int32, (W, Er), (Er, 1))
 
     def epochs(self):
         o = _lib.EpDispatchOutC()
@@ -255,6 +270,20 @@ class EpDispatchCombineOp:
         return self._combine_call(self.L.ep_combine_recv, input, weights,
                                   indices, out, out_weights, stream,
                                   "ep_combine_recv")
+
+    def moe_group(self, stream=None):
+        """Standard-MoE conversion: group the received rows per local expert.
+        Returns (grouped payload [W][gcap][H], grouped scales or None,
+        counts [W][Er], offsets [W][Er])."""
+        check(self.L.ep_moe_group(self.h, _stream(stream)), "ep_moe_group")
+        return self.moe_x, self.moe_x_scales, self.moe_count, self.moe_offset
+
+    def moe_ungroup(self, y=None, stream=None):
+        """Weighted per-row sums of the grouped expert outputs (y: None for the
+        registered moe_y buffer) into the registered combine input buffer."""
+        ys = 0 if y is None else y.stride(0) * 2
+        check(self.L.ep_moe_ungroup(self.h, _ptr(y), ys, _stream(stream)), "ep_moe_ungroup")
+        return self.combine_input
 
     def reset(self, stream=None):
         check(self.L.ep_reset(self.h, _stream(stream)), "ep_reset")

@@ -123,6 +123,10 @@ typedef struct {
                                          combine reads: EP_DT_BF16 (0) or
                                          EP_DT_FP32; the output is bf16 */
     int64_t wait_timeout_ns;          /* bound of every device wait; 0 = 1 s */
+    int32_t max_grouped_rows_per_rank;/* rows of the standard-MoE grouped
+                                         buffers per rank (0: no grouping);
+                                         cap * k is the exact worst case */
+    int32_t reserved1;
 } ep_config_t;
 
 typedef struct ep_handle ep_handle_t;
@@ -241,6 +245,42 @@ ep_status_t ep_combine(ep_handle_t *h, const void *d_y,
                        int64_t y_rank_stride_bytes, const float *d_w_in,
                        int64_t w_rank_stride_bytes, const int32_t *d_idx,
                        void *d_out, float *d_out_w, void *stream);
+
+/* Standard-MoE conversion ("Choosing an EP API and backend", EPv2 row:
+ * "standard-MoE conversion"), needs max_grouped_rows_per_rank > 0.
+ * After the receive phase of a dispatch, on every rank r the entries
+ * (received row p < min(recv_count[r], cap), top-k slot j) whose expert
+ * lives on r are grouped per local expert e = idx - r*Er: groups in e order,
+ * entries in (p, j) order inside a group.  count[r][e], offset[r][e] (its
+ * exclusive prefix) and entry_slot[r][p][j] (-1 if non-local) describe it;
+ * slot q of rank r gets the payload row (and FP8 scale row), g_src = p*k + j
+ * and g_w = the row's weight j.  Entries whose slot is >= the grouped
+ * capacity are dropped and set the CAPACITY bit. */
+typedef struct {
+    void     *xg;             /* [W] x [gcap][H] payload (bf16 or e4m3) */
+    float    *xg_scales;      /* [W] x [gcap][H/128] (FP8) or NULL */
+    int32_t  *g_src;          /* [W] x [gcap] p*k + j */
+    float    *g_w;            /* [W] x [gcap] routing weight of the entry */
+    void     *yg;             /* [W] x [gcap][H] bf16: registered expert-output rows */
+    int32_t  *entry_slot;     /* [W] x [cap][k] */
+    int64_t   rank_stride_bytes;
+    int32_t  *count;          /* [W][Er] */
+    int32_t  *offset;         /* [W][Er] */
+    int32_t   gcap;
+    int32_t   experts_per_rank;
+} ep_moe_out_t;
+
+ep_status_t ep_moe_group(ep_handle_t *h, void *stream);
+ep_status_t ep_moe_outputs(const ep_handle_t *h, ep_moe_out_t *out);
+
+/* The inverse before combine: for every received row p of rank r,
+ * y_r[p][h] = bf16_rne(+0.0f + sum over its entries j ascending of
+ * fl32(g_w * fp32(yg[slot][h]))) written to the registered combine input
+ * buffer (combine_dtype must be bf16).  d_yg: NULL for the registered
+ * expert-output buffer, else rank r's [gcap][H] bf16 rows at
+ * d_yg + r*yg_rank_stride_bytes.  BAD_STATE without a grouping. */
+ep_status_t ep_moe_ungroup(ep_handle_t *h, const void *d_yg,
+                           int64_t yg_rank_stride_bytes, void *stream);
 
 /* Reset between iterations: zero the ready flags, epochs and error word on
  * `stream` and forget the layout (combine then needs a new dispatch). */
