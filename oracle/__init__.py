@@ -86,6 +86,10 @@ def _declare(L):
         "or_group_rows": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P,
                                _P, _P, _P, _P]),
         "or_ungroup": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+        "or_identity_expert_fp8": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
+                                        _P, _P, _P, _P]),
+        "or_combine_fp8": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
+        "or_quant_block_f32": (None, [_P, _I, _P, _P]),
         "or_combine": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
         "or_combine_tokens": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _I,
                                    _P, _P]),
@@ -377,6 +381,49 @@ def ungroup(wl, recv_count, out_w, entry_slot, yg, cap, gcap):
                      _p(_c(out_w, np.float32)), _p(_c(entry_slot, np.int32)),
                      _p(_c(yg, np.uint16)), _p(y))
     return y
+
+
+def quant_rows_f32(v):
+    """Per-128-element-block FP8 quantisation of fp32 rows [n][H]."""
+    v = _c(v, np.float32)
+    n, H = v.shape
+    q = np.empty((n, H), np.uint8)
+    sc = np.empty((n, H // 128), np.float32)
+    for i in range(n):
+        for b in range(H // 128):
+            lib().or_quant_block_f32(v[i, b * 128:].ctypes.data_as(ctypes.c_void_p), 128,
+                                     q[i, b * 128:].ctypes.data_as(ctypes.c_void_p),
+                                     sc[i, b:].ctypes.data_as(ctypes.c_void_p))
+    return q, sc
+
+
+def identity_expert_fp8(wl, recv_count, payload, scales, out_w, out_idx, cap, fp8=None):
+    """Identity expert with an FP8 combine payload: (yq [W][cap][H],
+    ysc [W][cap][H/128]); rows past the count are zero."""
+    W, H, k = wl.world_size, wl.hidden, wl.topk
+    fp8 = wl.fp8 if fp8 is None else fp8
+    yq = np.zeros((W, cap, H), np.uint8)
+    ysc = np.zeros((W, cap, H // 128), np.float32)
+    sc = (_c(scales, np.float32) if fp8 else np.zeros((W, cap, 1), np.float32))
+    pl = _c(payload, np.uint8 if fp8 else np.uint16)
+    tmp = np.empty(H, np.float32)
+    lib().or_identity_expert_fp8(W, wl.num_experts, k, H, cap, int(fp8),
+                                 _p(_c(recv_count, np.int32)), _p(pl), _p(sc),
+                                 _p(_c(out_w, np.float32)), _p(_c(out_idx, np.int32)),
+                                 _p(tmp), _p(yq), _p(ysc))
+    return yq, ysc
+
+
+def combine_fp8(wl, num_tokens, pos, yq, ysc, w_in, cap):
+    """Combine of an FP8 expert payload -> bf16 out [W][T][H]."""
+    W, T, H, k = wl.world_size, wl.max_tokens_per_rank, wl.hidden, wl.topk
+    out = np.zeros((W, T, H), np.uint16)
+    out_w = np.zeros((W, T, k), np.float32) if w_in is not None else None
+    lib().or_combine_fp8(W, k, T, H, cap, _p(_c(num_tokens, np.int32)),
+                         _p(_c(pos, np.int32)), _p(_c(yq, np.uint8)), _p(_c(ysc, np.float32)),
+                         _p(None if w_in is None else _c(w_in, np.float32)),
+                         _p(out), _p(out_w))
+    return out, out_w
 
 
 def run_all(inp, cap=None):

@@ -675,3 +675,99 @@ int or_ungroup(int W, int k, int H, int cap, int gcap, const int32_t *recv_count
     }
     return OR_OK;
 }
+
+/* ---------------------------------------------- FP8 combine payload */
+
+/* One FP8 block of n fp32 values, the dispatch formula applied to fp32
+ * input: a = max |v_i|, scale = fl32(a / 448), q_i = E4M3(fl32(v_i / scale));
+ * a == 0 gives scale 0 and codes 0x00. */
+void or_quant_block_f32(const float *v, int n, uint8_t *q, float *scale)
+{
+    float a = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float m = fabsf(v[i]);
+        if (m > a) a = m;
+    }
+    if (a == 0.0f) {
+        *scale = 0.0f;
+        for (int i = 0; i < n; ++i) q[i] = 0x00;
+        return;
+    }
+    float s = a / 448.0f;
+    *scale = s;
+    for (int i = 0; i < n; ++i) q[i] = or_e4m3_encode(v[i] / s);
+}
+
+/* Identity expert writing an FP8 combine payload: the fp32 product
+ * fl32(v_h * alpha) of or_identity_expert_f32, quantised per 128-element
+ * block with or_quant_block_f32.  yq uint8 [W][cap][H], ysc [W][cap][H/128].
+ * Rows past min(recv_count, cap) are left as they are. */
+int or_identity_expert_fp8(int W, int E, int k, int H, int cap, int fp8,
+                           const int32_t *recv_count, const void *payload,
+                           const float *scales, const float *out_w,
+                           const int32_t *out_idx, float *tmp_row,
+                           uint8_t *yq, float *ysc)
+{
+    int Er = E / W;
+    int nb_in = fp8 ? H / 128 : 0;
+    int nb = H / 128;
+    for (int r = 0; r < W; ++r) {
+        int n = recv_count[r] < cap ? recv_count[r] : cap;
+        for (int p = 0; p < n; ++p) {
+            int64_t rp = (int64_t)r * cap + p;
+            float alpha = 0.0f;
+            for (int j = 0; j < k; ++j)
+                if (out_idx[rp * k + j] / Er == r)
+                    alpha = alpha + out_w[rp * k + j];
+            for (int h = 0; h < H; ++h) {
+                float v;
+                if (fp8)
+                    v = or_e4m3_value(((const uint8_t *)payload)[rp * H + h]) *
+                        scales[rp * nb_in + h / 128];
+                else
+                    v = or_bf16_to_f32(((const uint16_t *)payload)[rp * H + h]);
+                tmp_row[h] = v * alpha;
+            }
+            for (int b = 0; b < nb; ++b)
+                or_quant_block_f32(tmp_row + b * 128, 128, yq + rp * H + b * 128,
+                                   ysc + rp * nb + b);
+        }
+    }
+    return OR_OK;
+}
+
+/* Combine of an FP8 expert payload: out[s][t][h] = bf16_rne(+0.0f +
+ * sum over r in D(s,t) ascending of fl32(value(yq[r][p][h]) * ysc[r][p][h/128])),
+ * each product and '+' an fp32 operation; out_w as in or_combine. */
+int or_combine_fp8(int W, int k, int T, int H, int cap, const int32_t *num_tokens,
+                   const int32_t *pos, const uint8_t *yq, const float *ysc,
+                   const float *w_in, uint16_t *out, float *out_w)
+{
+    int nb = H / 128;
+    for (int s = 0; s < W; ++s)
+        for (int t = 0; t < num_tokens[s]; ++t) {
+            int64_t tok = (int64_t)s * T + t;
+            for (int h = 0; h < H; ++h) {
+                float acc = 0.0f;
+                for (int r = 0; r < W; ++r) {
+                    int32_t p = pos[tok * W + r];
+                    if (p < 0 || p >= cap) continue;
+                    int64_t rp = (int64_t)r * cap + p;
+                    float v = or_e4m3_value(yq[rp * H + h]) * ysc[rp * nb + h / 128];
+                    acc = acc + v;
+                }
+                out[tok * H + h] = or_bf16_rne(acc);
+            }
+            if (w_in && out_w)
+                for (int j = 0; j < k; ++j) {
+                    float acc = 0.0f;
+                    for (int r = 0; r < W; ++r) {
+                        int32_t p = pos[tok * W + r];
+                        if (p < 0 || p >= cap) continue;
+                        acc = acc + w_in[((int64_t)r * cap + p) * k + j];
+                    }
+                    out_w[tok * k + j] = acc;
+                }
+        }
+    return OR_OK;
+}

@@ -613,3 +613,61 @@ def test_grouped_identity_experts_give_back_the_input():
     assert np.all(np.abs(got - x) <= np.abs(x) * 2.0 ** -8 * 12)
     # every token's k selections land in exactly one group slot each
     assert count.sum() == wl.world_size * wl.max_tokens_per_rank * wl.topk
+
+
+# ------------------------------------------------- FP8 combine payload
+
+def test_fp8_quant_of_fp32_rows_matches_numpy_and_torch():
+    rng = np.random.default_rng(21)
+    v = (rng.standard_normal((20, 512)) * 2.0 ** rng.integers(-30, 30, size=(20, 1))).astype(np.float32)
+    v[3, :128] = 0.0
+    v[4, 5] = -0.0
+    q, sc = oracle.quant_rows_f32(v)
+    for i in range(20):
+        for b in range(4):
+            blk = v[i, b * 128:(b + 1) * 128]
+            a = np.float32(np.abs(blk).max())
+            if a == 0:
+                assert sc[i, b] == 0 and np.all(q[i, b * 128:(b + 1) * 128] == 0)
+                continue
+            s = np.float32(a / np.float32(448))
+            assert sc[i, b] == s
+            assert np.array_equal(q[i, b * 128:(b + 1) * 128],
+                                  bf.torch_e4m3((blk / s).astype(np.float32)))
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_fp8_combine_payload_matches_bruteforce(fp8):
+    rng = np.random.default_rng(1000 + int(fp8))
+    wl, inp = _random_case(rng, 4, 2, 3, 10, 256, fp8=fp8)
+    res = oracle.run_all(inp)
+    W, T, H, cap = wl.world_size, wl.max_tokens_per_rank, wl.hidden, res["cap"]
+    yq, ysc = oracle.identity_expert_fp8(wl, res["recv_count"], res["out"], res["out_scales"],
+                                         res["out_w"], res["out_idx"], cap)
+    y32 = oracle.identity_expert_f32(wl, res["recv_count"], res["out"], res["out_scales"],
+                                     res["out_w"], res["out_idx"], cap)
+    for r in range(W):
+        n = res["recv_count"][r]
+        if n:
+            q2, s2 = oracle.quant_rows_f32(y32[r, :n])
+            assert np.array_equal(yq[r, :n], q2) and np.array_equal(ysc[r, :n], s2)
+    deq = (bf.torch_e4m3_value(yq) * np.repeat(ysc, 128, axis=2)).astype(np.float32)
+    disp = bf.dispatch(inp.x_bits, inp.weights, inp.indices, inp.num_tokens, W,
+                       wl.num_experts, fp8=fp8)
+    ys = {r: [deq[r, i] for i in range(len(disp[r]["rows"]))] for r in range(W)}
+    exp = bf.combine_f32(disp, ys, W, T, H, inp.num_tokens)
+    got, _ = oracle.combine_fp8(wl, inp.num_tokens, res["pos"], yq, ysc, None, cap)
+    for (s, t), row in exp.items():
+        assert np.array_equal(got[s, t], row)
+    # identity closed form: within the E4M3 step of the combined rows
+    x = bf.to_f32(inp.x_bits)
+    if fp8:
+        q, s = oracle.quant_rows(inp.x_bits.reshape(-1, H))
+        x = (oracle.e4m3_value(q) * np.repeat(s, 128, axis=1)).reshape(x.shape)
+    o = bf.to_f32(got)
+    for s_ in range(W):
+        n = inp.num_tokens[s_]
+        if n == 0:
+            continue
+        assert np.all(np.abs(o[s_, :n] - x[s_, :n]) <= np.abs(x[s_, :n]) * 0.2 +
+                      np.abs(x[s_, :n]).max() * 2.0 ** -9)
