@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kGroupWarps * 32) moe_group_kernel(const MoePa
     }
 }
 
-template <int MAXE>
+template <int MAXE, int U>
 __global__ void __launch_bounds__(kMoeWarps * 32) moe_ungroup_kernel(const MoeParams p,
                                                                      const char *yg,
                                                                      int64_t yg_stride) {
@@ -256,34 +256,42 @@ __global__ void __launch_bounds__(kMoeWarps * 32) moe_ungroup_kernel(const MoePa
         }
     }
     uint4 *out = reinterpret_cast<uint4 *>(const_cast<char *>(seg) + p.off_comb) + (int64_t)row * nvec;
-    for (int v = lane; v < nvec; v += 32) {
-        uint4 val[MAXE];
+    // U column vectors per lane per pass: up to U * MAXE loads in flight
+    for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+        uint4 val[U][MAXE];
 #pragma unroll
         for (int i = 0; i < MAXE; ++i)
-            if (i < ne) val[i] = ld_stream16(rows[i] + (int64_t)v * 16);
-        float acc[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+            for (int u = 0; u < U; ++u)
+                if (i < ne && v0 + 32 * u < nvec)
+                    val[u][i] = ld_stream16(rows[i] + (int64_t)(v0 + 32 * u) * 16);
 #pragma unroll
-        for (int i = 0; i < MAXE; ++i) {
-            if (i < ne) {
-                const uint32_t wd[4] = {val[i].x, val[i].y, val[i].z, val[i].w};
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + 32 * u;
+            if (v >= nvec) continue;
+            float acc[8];
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    acc[2 * h] = __fadd_rn(acc[2 * h], __fmul_rn(ws[i], __uint_as_float(wd[h] << 16)));
-                    acc[2 * h + 1] = __fadd_rn(acc[2 * h + 1],
-                                               __fmul_rn(ws[i], __uint_as_float(wd[h] & 0xffff0000u)));
+            for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll
+            for (int i = 0; i < MAXE; ++i) {
+                if (i < ne) {
+                    const uint32_t wd[4] = {val[u][i].x, val[u][i].y, val[u][i].z, val[u][i].w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        acc[2 * h] = __fadd_rn(acc[2 * h],
+                                               __fmul_rn(ws[i], __uint_as_float(wd[h] << 16)));
+                        acc[2 * h + 1] = __fadd_rn(
+                            acc[2 * h + 1], __fmul_rn(ws[i], __uint_as_float(wd[h] & 0xffff0000u)));
+                    }
                 }
             }
-        }
-        uint4 o;
-        uint32_t pk[4];
+            uint32_t pk[4];
 #pragma unroll
-        for (int h = 0; h < 4; ++h)
-            pk[h] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * h])) |
-                    ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * h + 1])) << 16);
-        o = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        out[v] = o;
+            for (int h = 0; h < 4; ++h)
+                pk[h] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * h])) |
+                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * h + 1])) << 16);
+            st_stream16(out + v, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+        }
     }
 }
 
@@ -330,11 +338,11 @@ cudaError_t launch_moe_ungroup(const Config &c, const Workspace &ws, const char 
     const MoeParams p = make_params(c, ws);
     const int64_t rows = (int64_t)c.W * c.cap;
     const int blocks = (int)((rows + kMoeWarps - 1) / kMoeWarps);
-    if (c.k <= 2) moe_ungroup_kernel<2><<<blocks, kMoeWarps * 32, 0, st>>>(p, yg, yg_stride);
-    else if (c.k <= 4) moe_ungroup_kernel<4><<<blocks, kMoeWarps * 32, 0, st>>>(p, yg, yg_stride);
-    else if (c.k <= 8) moe_ungroup_kernel<8><<<blocks, kMoeWarps * 32, 0, st>>>(p, yg, yg_stride);
-    else if (c.k <= 16) moe_ungroup_kernel<16><<<blocks, kMoeWarps * 32, 0, st>>>(p, yg, yg_stride);
-    else moe_ungroup_kernel<32><<<blocks, kMoeWarps * 32, 0, st>>>(p, yg, yg_stride);
+    if (c.k <= 2) moe_ungroup_kernel<2, 4><<<blocks, kMoeWarps * 32, 0, st>>>(p, yg, yg_stride);
+    else if (c.k <= 4) moe_ungroup_kernel<4, 4><<<blocks, kMoeWarps * 32, 0, st>>>(p, yg, yg_stride);
+    else if (c.k <= 8) moe_ungroup_kernel<8, 2><<<blocks, kMoeWarps * 32, 0, st>>>(p, yg, yg_stride);
+    else if (c.k <= 16) moe_ungroup_kernel<16, 1><<<blocks, kMoeWarps * 32, 0, st>>>(p, yg, yg_stride);
+    else moe_ungroup_kernel<32, 1><<<blocks, kMoeWarps * 32, 0, st>>>(p, yg, yg_stride);
     return cudaGetLastError();
 }
 
