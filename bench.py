@@ -57,7 +57,7 @@ def parse():
                     help="receive rows per rank (0: W*T)")
     ap.add_argument("--fp8-input", action="store_true",
                     help="FP8 workloads: dispatch a pre-quantised payload (codes + scales)")
-    ap.add_argument("--combine-dtype", choices=["bf16", "fp32"], default="bf16",
+    ap.add_argument("--combine-dtype", choices=["bf16", "fp32", "fp8_e4m3"], default="bf16",
                     help="element type of the expert rows combine reads")
     ap.add_argument("--moe-group", type=int, default=0, metavar="GCAP",
                     help="also time the standard-MoE grouping / un-grouping with "
@@ -242,12 +242,13 @@ def run_ours(args, rank, world, local_rank):
     else:
         xs = x.float()
     ys = out.float()
-    if xsc is not None:
-        ident_ok = bool(((ys - xs).abs() <= xs.abs() * (2.0 ** -8 * 10) + 1e-30).all())
-    elif wl.fp8:
-        ident_ok = bool(((ys - xs).abs() <= xs.abs() * 0.07 + 1e-2).all())
+    # tolerance: bf16 rounding of the expert product and of the sum; an E4M3
+    # step (2^-4 relative) where a payload is quantised on the way
+    quantised = (wl.fp8 and xsc is None) or args.combine_dtype == "fp8_e4m3"
+    if quantised:
+        ident_ok = bool(((ys - xs).abs() <= xs.abs() * 0.15 + xs.abs().amax() * 2.0 ** -8).all())
     else:
-        ident_ok = bool(((ys - xs).abs() <= xs.abs() * (2.0 ** -8 * 10)).all())
+        ident_ok = bool(((ys - xs).abs() <= xs.abs() * (2.0 ** -8 * 10) + 1e-30).all())
     st, mask = op.get_error(stream)
     ident_ok = ident_ok and st == 0
     del xs, ys
@@ -306,7 +307,7 @@ def run_ours(args, rank, world, local_rank):
     value = world * N / (ms_per_step / 1e3)
 
     ab = algorithmic_bytes(wl, P, N, wl.fp8, fp8_input=args.fp8_input,
-                           y_bytes=4 if args.combine_dtype == "fp32" else 2)
+                           y_bytes={"fp32": 4, "bf16": 2, "fp8_e4m3": 1 + 4 / 128}[args.combine_dtype])
     step_bytes = ab["dispatch"] + ab["combine"]
     peak, peak_kind = measured_peak()
     d_ms, c_ms = float(dis.mean()), float(com.mean())

@@ -106,6 +106,7 @@ SIGNATURES = {
     "ep_dispatch_send_replay": (_S, [_P, _P, _P, _P, _P, _P, _P]),
     "ep_dispatch_outputs": (_S, [_P, ctypes.POINTER(EpDispatchOutC)]),
     "ep_get_combine_input_buffer": (_S, [_P, _I32, ctypes.POINTER(_P), ctypes.POINTER(_I64)]),
+    "ep_get_combine_input_scales": (_S, [_P, ctypes.POINTER(_P), ctypes.POINTER(_I64)]),
     "ep_combine_send": (_S, [_P, _P]),
     "ep_combine_recv": (_S, [_P, _P, _I64, _P, _I64, _P, _P, _P, _P]),
     "ep_combine": (_S, [_P, _P, _I64, _P, _I64, _P, _P, _P, _P]),

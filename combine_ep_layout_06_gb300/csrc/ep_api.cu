@@ -38,7 +38,10 @@ ep_status_t make_config(const ep_config_t *in, Config *c) {
     if (in->dispatch_dtype != EP_DT_BF16 && in->dispatch_dtype != EP_DT_FP8_E4M3)
         return EP_ERR_INVALID_ARGS;
     const bool fp8 = in->dispatch_dtype == EP_DT_FP8_E4M3;
-    if (in->combine_dtype != EP_DT_BF16 && in->combine_dtype != EP_DT_FP32)
+    if (in->combine_dtype != EP_DT_BF16 && in->combine_dtype != EP_DT_FP32 &&
+        in->combine_dtype != EP_DT_FP8_E4M3)
+        return EP_ERR_INVALID_ARGS;
+    if (in->combine_dtype == EP_DT_FP8_E4M3 && H % EP_QUANT_BLOCK != 0)
         return EP_ERR_INVALID_ARGS;
     if (fp8 && (H % EP_QUANT_BLOCK != 0 || H > 16384)) return EP_ERR_INVALID_ARGS;
     const int64_t cap = in->max_recv_tokens_per_rank > 0
@@ -51,6 +54,7 @@ ep_status_t make_config(const ep_config_t *in, Config *c) {
     c->cap = (int)cap;
     c->fp8 = fp8;
     c->y_f32 = in->combine_dtype == EP_DT_FP32;
+    c->y_fp8 = in->combine_dtype == EP_DT_FP8_E4M3;
     c->nch = (T + kChunk - 1) / kChunk;
     c->G = W * c->nch;
     c->Q = (c->G + kGroup - 1) / kGroup;
@@ -127,7 +131,8 @@ void plan_workspace(const Config &c, char *base, Workspace *ws) {
     ws->off_w = seg_take(cap * k * 4);
     ws->off_idx = seg_take(cap * k * 4);
     ws->off_src = seg_take(cap * 4);
-    ws->off_comb = seg_take(cap * H * (c.y_f32 ? 4 : 2));
+    ws->off_comb = seg_take(cap * H * (c.y_f32 ? 4 : (c.y_fp8 ? 1 : 2)));
+    ws->off_comb_sc = seg_take(c.y_fp8 ? cap * (H / EP_QUANT_BLOCK) * 4 : 0);
     const size_t gc = c.gcap;
     ws->off_xg = seg_take(gc * H * (c.fp8 ? 1 : 2));
     ws->off_xgs = seg_take(c.fp8 ? gc * c.nb * 4 : 0);
@@ -368,8 +373,18 @@ ep_status_t ep_dispatch_outputs(const ep_handle_t *h, ep_dispatch_out_t *o) {
 ep_status_t ep_get_combine_input_buffer(const ep_handle_t *h, int32_t dtype,
                                         void **d_ptr, int64_t *rank_stride_bytes) {
     if (!h || !d_ptr || !rank_stride_bytes) return EP_ERR_INVALID_ARGS;
-    if (dtype != (h->cfg.y_f32 ? EP_DT_FP32 : EP_DT_BF16)) return EP_ERR_NOT_FOUND;
+    if (dtype != (h->cfg.y_f32 ? EP_DT_FP32 : (h->cfg.y_fp8 ? EP_DT_FP8_E4M3 : EP_DT_BF16)))
+        return EP_ERR_NOT_FOUND;
     *d_ptr = h->ws.seg0 + h->ws.off_comb;
+    *rank_stride_bytes = h->ws.seg_stride;
+    return EP_SUCCESS;
+}
+
+ep_status_t ep_get_combine_input_scales(const ep_handle_t *h, float **d_ptr,
+                                        int64_t *rank_stride_bytes) {
+    if (!h || !d_ptr || !rank_stride_bytes) return EP_ERR_INVALID_ARGS;
+    if (!h->cfg.y_fp8) return EP_ERR_NOT_FOUND;
+    *d_ptr = reinterpret_cast<float *>(h->ws.seg0 + h->ws.off_comb_sc);
     *rank_stride_bytes = h->ws.seg_stride;
     return EP_SUCCESS;
 }
@@ -399,6 +414,8 @@ static ep_status_t combine_args(ep_handle_t *h, const void *d_y, int64_t y_strid
     if (d_idx && !aligned(d_idx, 4)) return EP_ERR_INVALID_ARGS;
     if ((d_w_in == nullptr) != (d_out_w == nullptr)) return EP_ERR_INVALID_ARGS;
     const int64_t row_bytes = (int64_t)c.cap * c.H * (c.y_f32 ? 4 : 2);
+    a->ysc = h->ws.seg0 + h->ws.off_comb_sc;
+    if (d_y && c.y_fp8) return EP_ERR_INVALID_ARGS;   // FP8 payload: registered buffer only
     if (d_y) {
         if (y_stride == 0) y_stride = row_bytes;
         if (!aligned(d_y, 16) || y_stride % 16 != 0 || y_stride < row_bytes)
@@ -510,7 +527,7 @@ ep_status_t ep_moe_ungroup(ep_handle_t *h, const void *d_yg, int64_t yg_stride,
                            void *stream) {
     if (!h) return EP_ERR_INVALID_ARGS;
     const Config &c = h->cfg;
-    if (c.gcap <= 0 || c.y_f32) return EP_ERR_INVALID_ARGS;
+    if (c.gcap <= 0 || c.y_f32 || c.y_fp8) return EP_ERR_INVALID_ARGS;
     const int64_t rows = (int64_t)c.gcap * c.H * 2;
     const char *yg;
     if (d_yg) {
@@ -572,6 +589,7 @@ ep_status_t ep_test_identity_expert(ep_handle_t *h, void *d_y,
     if (!h) return EP_ERR_INVALID_ARGS;
     if (!h->layout_valid) return EP_ERR_BAD_STATE;
     const int64_t row_bytes = (int64_t)h->cfg.cap * h->cfg.H * (h->cfg.y_f32 ? 4 : 2);
+    if (d_y && h->cfg.y_fp8) return EP_ERR_INVALID_ARGS;
     char *y;
     int64_t ys;
     if (d_y) {

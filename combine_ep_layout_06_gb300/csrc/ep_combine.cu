@@ -9,14 +9,16 @@
 // expert outputs back"; combine_send()/combine_recv(); and the "AsyncLL v2
 // SDMA overlap" section for the split receive): out[s][t] = bf16_rne(
 // +0.0f + y_r0[p0] + y_r1[p1] + ...) over r in D(s,t) ascending, each '+' an
-// fp32 add.
+// fp32 add.  The expert rows are bf16, fp32, or E4M3 codes with one fp32
+// scale per 128 elements (each element then enters as fl32(value(q)*scale)).
 //
 // GB300 mapping.  One warp per source token.  Lanes read the token's W
-// slots; for each group of U 16-byte column vectors a lane issues the loads
-// of ALL of the token's (<= MAXD) rows before it adds any, so up to
-// U * MAXD independent 16-byte loads per lane are in flight, then it adds
+// slots; for each group of U column vectors (8 output elements each) a lane
+// issues the loads of ALL of the token's (<= MAXD) rows before it adds any,
+// so up to U * MAXD independent loads per lane are in flight, then it adds
 // them in rank order and writes 16 bytes of bf16.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include "ep_device.cuh"
@@ -37,8 +39,12 @@ namespace {
 constexpr int kCombineWarps = EP_COMBINE_WARPS;
 constexpr int kCombineThreads = kCombineWarps * 32;
 
+// Kind of expert row combine reads.
+constexpr int kYBf16 = 0, kYF32 = 1, kYFp8 = 2;
+
 struct CombineParams {
     const char *y;
+    const char *ysc;          // FP8 rows: block scales, same rank stride as y
     int64_t y_stride;
     const char *w_in;
     int64_t w_stride;
@@ -48,7 +54,7 @@ struct CombineParams {
     float *out_w;
     uint32_t *words;
     const uint32_t *cflags;
-    int W, E, Er, k, T, cap, nvec;
+    int W, E, Er, k, T, cap, nvec, nb;
     int fused_wait;
     uint32_t epoch;
     int64_t timeout_ns;
@@ -63,6 +69,18 @@ __device__ __forceinline__ uint4 ld_coherent16(const void *p) {
                  : "memory");
     return v;
 }
+__device__ __forceinline__ uint2 ld_stream8(const void *p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ld_coherent8(const void *p) {
+    uint2 v;
+    asm volatile("ld.global.cs.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+    return v;
+}
 
 __device__ __forceinline__ void add_bf16x8(float acc[8], const uint4 &v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -70,6 +88,33 @@ __device__ __forceinline__ void add_bf16x8(float acc[8], const uint4 &v) {
     for (int i = 0; i < 4; ++i) {
         acc[2 * i] = acc[2 * i] + __uint_as_float(w[i] << 16);
         acc[2 * i + 1] = acc[2 * i + 1] + __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ void add_f32x4(float *acc, const uint4 &v) {
+    acc[0] = acc[0] + __uint_as_float(v.x);
+    acc[1] = acc[1] + __uint_as_float(v.y);
+    acc[2] = acc[2] + __uint_as_float(v.z);
+    acc[3] = acc[3] + __uint_as_float(v.w);
+}
+
+// Values of 2 E4M3 codes (exact in half, hence in float).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+    return __half22float2(__half2(h));
+}
+
+// acc += fl32(value(q) * scale) for 8 codes (no fused multiply-add).
+__device__ __forceinline__ void add_fp8x8(float acc[8], const uint2 &q, float scale) {
+    const uint32_t w[2] = {q.x, q.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float2 lo = e4m3x2_to_float2(w[i] & 0xffffu);
+        const float2 hi = e4m3x2_to_float2(w[i] >> 16);
+        acc[4 * i + 0] = __fadd_rn(acc[4 * i + 0], __fmul_rn(lo.x, scale));
+        acc[4 * i + 1] = __fadd_rn(acc[4 * i + 1], __fmul_rn(lo.y, scale));
+        acc[4 * i + 2] = __fadd_rn(acc[4 * i + 2], __fmul_rn(hi.x, scale));
+        acc[4 * i + 3] = __fadd_rn(acc[4 * i + 3], __fmul_rn(hi.y, scale));
     }
 }
 
@@ -98,18 +143,48 @@ __device__ void fused_receive_wait(const CombineParams &p) {
     __syncthreads();
 }
 
-__device__ __forceinline__ void add_f32x4(float *acc, const uint4 &v) {
-    acc[0] = acc[0] + __uint_as_float(v.x);
-    acc[1] = acc[1] + __uint_as_float(v.y);
-    acc[2] = acc[2] + __uint_as_float(v.z);
-    acc[3] = acc[3] + __uint_as_float(v.w);
+// One row's share of a column vector: bf16 = one 16-byte load, fp32 = two,
+// FP8 = 8 code bytes plus the block scale (in a.z).
+struct RowVec {
+    uint4 a;
+    uint4 b;
+};
+
+template <int YK, bool COHERENT>
+__device__ __forceinline__ RowVec load_vec(const char *row, const char *srow, int v) {
+    RowVec r;
+    if constexpr (YK == kYBf16) {
+        r.a = COHERENT ? ld_coherent16(row + (int64_t)v * 16) : ld_stream16(row + (int64_t)v * 16);
+    } else if constexpr (YK == kYF32) {
+        r.a = COHERENT ? ld_coherent16(row + (int64_t)v * 32) : ld_stream16(row + (int64_t)v * 32);
+        r.b = COHERENT ? ld_coherent16(row + (int64_t)v * 32 + 16)
+                       : ld_stream16(row + (int64_t)v * 32 + 16);
+    } else {
+        const uint2 q = COHERENT ? ld_coherent8(row + (int64_t)v * 8) : ld_stream8(row + (int64_t)v * 8);
+        r.a.x = q.x;
+        r.a.y = q.y;
+        r.a.z = __float_as_uint(reinterpret_cast<const float *>(srow)[v >> 4]);
+    }
+    return r;
 }
 
-// F32: the expert rows are fp32 (two 16-byte loads per 8 output elements).
-template <int MAXD, int U, bool COHERENT, bool F32>
+template <int YK>
+__device__ __forceinline__ void add_vec(float acc[8], const RowVec &r) {
+    if constexpr (YK == kYBf16) {
+        add_bf16x8(acc, r.a);
+    } else if constexpr (YK == kYF32) {
+        add_f32x4(acc, r.a);
+        add_f32x4(acc + 4, r.b);
+    } else {
+        add_fp8x8(acc, make_uint2(r.a.x, r.a.y), __uint_as_float(r.a.z));
+    }
+}
+
+template <int MAXD, int U, bool COHERENT, int YK>
 __global__ void __launch_bounds__(kCombineThreads, EP_COMBINE_MIN_BLOCKS)
 combine_kernel(const CombineParams p) {
-    constexpr int NL = F32 ? 2 : 1;       // 16-byte loads per output vector
+    // bytes of one column vector of an expert row: bf16 16, fp32 32, FP8 8
+    constexpr int VB = YK == kYF32 ? 32 : (YK == kYFp8 ? 8 : 16);
     if (p.fused_wait) fused_receive_wait(p);
 
     const int lane = threadIdx.x & 31;
@@ -135,17 +210,21 @@ combine_kernel(const CombineParams p) {
 
     // rows of this token, ranks ascending
     const char *rows[MAXD];
+    const char *srows[MAXD];
     int nd = 0;
     {
         uint32_t mm = dm;
 #pragma unroll
         for (int j = 0; j < MAXD; ++j) {
             rows[j] = nullptr;
+            srows[j] = nullptr;
             if (mm) {
                 const int r = __ffs(mm) - 1;
                 mm &= mm - 1u;
                 const int slot = __shfl_sync(0xffffffffu, pr, r);
-                rows[j] = p.y + (int64_t)r * p.y_stride + (int64_t)slot * p.nvec * 16 * NL;
+                rows[j] = p.y + (int64_t)r * p.y_stride + (int64_t)slot * p.nvec * VB;
+                if constexpr (YK == kYFp8)
+                    srows[j] = p.ysc + (int64_t)r * p.y_stride + (int64_t)slot * p.nb * 4;
                 nd = j + 1;
             }
         }
@@ -153,20 +232,14 @@ combine_kernel(const CombineParams p) {
 
     uint4 *out_row = reinterpret_cast<uint4 *>(p.out) + tok * p.nvec;
     for (int v0 = lane; v0 < p.nvec; v0 += 32 * U) {
-        uint4 val[U][MAXD][NL];
+        RowVec val[U][MAXD];
 #pragma unroll
         for (int j = 0; j < MAXD; ++j) {
             if (j < nd) {
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int v = v0 + 32 * u;
-                    if (v < p.nvec) {
-#pragma unroll
-                        for (int l = 0; l < NL; ++l) {
-                            const char *a = rows[j] + ((int64_t)v * NL + l) * 16;
-                            val[u][j][l] = COHERENT ? ld_coherent16(a) : ld_stream16(a);
-                        }
-                    }
+                    if (v < p.nvec) val[u][j] = load_vec<YK, COHERENT>(rows[j], srows[j], v);
                 }
             }
         }
@@ -178,16 +251,8 @@ combine_kernel(const CombineParams p) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
 #pragma unroll
-            for (int j = 0; j < MAXD; ++j) {
-                if (j < nd) {
-                    if constexpr (F32) {
-                        add_f32x4(acc, val[u][j][0]);
-                        add_f32x4(acc + 4, val[u][j][1]);
-                    } else {
-                        add_bf16x8(acc, val[u][j][0]);
-                    }
-                }
-            }
+            for (int j = 0; j < MAXD; ++j)
+                if (j < nd) add_vec<YK>(acc, val[u][j]);
             uint4 o;
             o.x = pack_bf16x2(acc[0], acc[1]);
             o.y = pack_bf16x2(acc[2], acc[3]);
@@ -222,47 +287,76 @@ __global__ void flags_wait_kernel(const uint32_t *flags, uint32_t *words,
         set_error(words, EP_DEVERR_TIMEOUT);
 }
 
-// Identity expert: warp per received row.
-__global__ void __launch_bounds__(256)
-identity_expert_kernel(const char *seg0, int64_t seg_stride, int64_t off_out,
-                       int64_t off_scales, int64_t off_w, int64_t off_idx,
-                       const int32_t *totals, char *y, int64_t y_stride,
-                       int W, int E, int Er, int k, int H, int cap, int fp8,
-                       int y_f32) {
+// 8 fp32 values -> 8 E4M3 codes given the block scale.
+__device__ __forceinline__ uint2 quant8_f32(const float g[8], float scale) {
+    uint32_t w[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t packed = 0;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float a = g[4 * h + 2 * i] / scale;
+            const float b = g[4 * h + 2 * i + 1] / scale;
+            const __nv_fp8x2_storage_t q =
+                __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+            packed |= (uint32_t)q << (16 * i);
+        }
+        w[h] = packed;
+    }
+    return make_uint2(w[0], w[1]);
+}
+
+// Identity expert (test harness): warp per received row.
+struct IdentityParams {
+    const char *seg0;
+    int64_t seg_stride, off_out, off_scales, off_w, off_idx;
+    const int32_t *totals;
+    char *y;
+    char *ysc;               // FP8 payload scales (registered buffer)
+    int64_t y_stride;
+    int W, E, Er, k, H, cap, fp8, yk;
+};
+
+__global__ void __launch_bounds__(256) identity_expert_kernel(const IdentityParams a) {
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int r = (int)(gw / cap);
-    const int slot = (int)(gw - (int64_t)r * cap);
-    if (r >= W) return;
-    if (slot >= min(totals[r], cap)) return;
-    const char *seg = seg0 + (int64_t)r * seg_stride;
-    const float *wrow = reinterpret_cast<const float *>(seg + off_w) + (int64_t)slot * k;
-    const int32_t *irow = reinterpret_cast<const int32_t *>(seg + off_idx) + (int64_t)slot * k;
+    const int r = (int)(gw / a.cap);
+    const int slot = (int)(gw - (int64_t)r * a.cap);
+    if (r >= a.W) return;
+    if (slot >= min(a.totals[r], a.cap)) return;
+    const char *seg = a.seg0 + (int64_t)r * a.seg_stride;
+    const float *wrow = reinterpret_cast<const float *>(seg + a.off_w) + (int64_t)slot * a.k;
+    const int32_t *irow = reinterpret_cast<const int32_t *>(seg + a.off_idx) + (int64_t)slot * a.k;
     float alpha = 0.0f;
-    for (int j = 0; j < k; ++j) {
+    for (int j = 0; j < a.k; ++j) {
         const int32_t e = irow[j];
-        if ((uint32_t)e < (uint32_t)E && e / Er == r) alpha = alpha + wrow[j];
+        if ((uint32_t)e < (uint32_t)a.E && e / a.Er == r) alpha = alpha + wrow[j];
     }
-    const int nvec = H / 8;
-    uint4 *yrow = reinterpret_cast<uint4 *>(y + (int64_t)r * y_stride) +
-                  (int64_t)slot * nvec * (y_f32 ? 2 : 1);
-    for (int v = lane; v < nvec; v += 32) {
+    const int nvec = a.H / 8;
+    const int vb = a.yk == kYF32 ? 32 : (a.yk == kYFp8 ? 8 : 16);
+    char *yrow = a.y + (int64_t)r * a.y_stride + (int64_t)slot * nvec * vb;
+    // warp-uniform trip count: the FP8 output shuffles for the block amax
+    for (int base = 0; base < nvec; base += 32) {
+        const int v = base + lane;
+        const bool active = v < nvec;
         float f[8];
-        if (fp8) {
+        if (!active) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = 0.f;
+        } else if (a.fp8) {
             const uint2 q = *reinterpret_cast<const uint2 *>(
-                seg + off_out + (int64_t)slot * H + (int64_t)v * 8);
-            const float sc = reinterpret_cast<const float *>(seg + off_scales)
-                [(int64_t)slot * (H / 128) + (v >> 4)];
+                seg + a.off_out + (int64_t)slot * a.H + (int64_t)v * 8);
+            const float sc = reinterpret_cast<const float *>(seg + a.off_scales)
+                [(int64_t)slot * (a.H / 128) + (v >> 4)];
             const uint32_t qw[2] = {q.x, q.y};
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const __nv_fp8_storage_t code = (qw[e >> 2] >> (8 * (e & 3))) & 0xffu;
                 const __half_raw hr = __nv_cvt_fp8_to_halfraw(code, __NV_E4M3);
-                const float val = __half2float(__half(hr));
-                f[e] = val * sc;
+                f[e] = __half2float(__half(hr)) * sc;
             }
         } else {
-            const uint4 raw = reinterpret_cast<const uint4 *>(seg + off_out)[(int64_t)slot * nvec + v];
+            const uint4 raw = reinterpret_cast<const uint4 *>(seg + a.off_out)[(int64_t)slot * nvec + v];
             const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -270,44 +364,68 @@ identity_expert_kernel(const char *seg0, int64_t seg_stride, int64_t off_out,
                 f[2 * i + 1] = __uint_as_float(w4[i] & 0xffff0000u);
             }
         }
-        if (y_f32) {
-            float g[8];
+        float g[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) g[e] = f[e] * alpha;
-            yrow[2 * v] = make_uint4(__float_as_uint(g[0]), __float_as_uint(g[1]),
-                                     __float_as_uint(g[2]), __float_as_uint(g[3]));
-            yrow[2 * v + 1] = make_uint4(__float_as_uint(g[4]), __float_as_uint(g[5]),
-                                         __float_as_uint(g[6]), __float_as_uint(g[7]));
-        } else {
+        for (int e = 0; e < 8; ++e) g[e] = f[e] * alpha;
+        if (a.yk == kYF32) {
+            if (active) {
+                uint4 *d = reinterpret_cast<uint4 *>(yrow) + 2 * v;
+                d[0] = make_uint4(__float_as_uint(g[0]), __float_as_uint(g[1]),
+                                  __float_as_uint(g[2]), __float_as_uint(g[3]));
+                d[1] = make_uint4(__float_as_uint(g[4]), __float_as_uint(g[5]),
+                                  __float_as_uint(g[6]), __float_as_uint(g[7]));
+            }
+        } else if (a.yk == kYFp8) {
+            // 16 lanes x 8 elements = one 128-element block
+            float am = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(g[e]));
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+            float scale = 0.f;
+            uint2 q = make_uint2(0u, 0u);
+            if (am != 0.f) {
+                scale = am / 448.0f;
+                q = quant8_f32(g, scale);
+            }
+            if (active) {
+                reinterpret_cast<uint2 *>(yrow)[v] = q;
+                if ((lane & 15) == 0)
+                    reinterpret_cast<float *>(a.ysc + (int64_t)r * a.y_stride)
+                        [(int64_t)slot * (a.H / 128) + (v >> 4)] = scale;
+            }
+        } else if (active) {
             uint4 o;
-            o.x = pack_bf16x2(f[0] * alpha, f[1] * alpha);
-            o.y = pack_bf16x2(f[2] * alpha, f[3] * alpha);
-            o.z = pack_bf16x2(f[4] * alpha, f[5] * alpha);
-            o.w = pack_bf16x2(f[6] * alpha, f[7] * alpha);
-            yrow[v] = o;
+            o.x = pack_bf16x2(g[0], g[1]);
+            o.y = pack_bf16x2(g[2], g[3]);
+            o.z = pack_bf16x2(g[4], g[5]);
+            o.w = pack_bf16x2(g[6], g[7]);
+            reinterpret_cast<uint4 *>(yrow)[v] = o;
         }
     }
 }
 
-template <int MAXD, int U, bool COH, bool F32>
+template <int MAXD, int U, bool COH, int YK>
 cudaError_t launch_combine_t(const Config &c, const CombineParams &p,
                              cudaStream_t st) {
     const int64_t tokens = (int64_t)c.W * c.T;
     const int blocks = (int)((tokens + kCombineWarps - 1) / kCombineWarps);
-    combine_kernel<MAXD, U, COH, F32><<<blocks, kCombineThreads, 0, st>>>(p);
+    combine_kernel<MAXD, U, COH, YK><<<blocks, kCombineThreads, 0, st>>>(p);
     return cudaGetLastError();
+}
+
+template <int MAXD, int U, int YK>
+cudaError_t launch_combine_y(const Config &c, const CombineParams &p, cudaStream_t st) {
+    if (p.fused_wait) return launch_combine_t<MAXD, U, true, YK>(c, p, st);
+    return launch_combine_t<MAXD, U, false, YK>(c, p, st);
 }
 
 template <int MAXD, int U>
 cudaError_t launch_combine_m(const Config &c, const CombineParams &p,
                              cudaStream_t st) {
-    if (c.y_f32) {
-        constexpr int U32 = U > 1 ? U / 2 : 1;    // twice the bytes per vector
-        if (p.fused_wait) return launch_combine_t<MAXD, U32, true, true>(c, p, st);
-        return launch_combine_t<MAXD, U32, false, true>(c, p, st);
-    }
-    if (p.fused_wait) return launch_combine_t<MAXD, U, true, false>(c, p, st);
-    return launch_combine_t<MAXD, U, false, false>(c, p, st);
+    if (c.y_f32) return launch_combine_y<MAXD, (U > 1 ? U / 2 : 1), kYF32>(c, p, st);
+    if (c.y_fp8) return launch_combine_y<MAXD, U, kYFp8>(c, p, st);
+    return launch_combine_y<MAXD, U, kYBf16>(c, p, st);
 }
 
 }  // namespace
@@ -316,6 +434,7 @@ cudaError_t launch_combine(const Config &c, const Workspace &ws,
                            const CombineArgs &a, cudaStream_t st) {
     CombineParams p;
     p.y = a.y;
+    p.ysc = a.ysc;
     p.y_stride = a.y_stride;
     p.w_in = a.w_in;
     p.w_stride = a.w_stride;
@@ -327,6 +446,7 @@ cudaError_t launch_combine(const Config &c, const Workspace &ws,
     p.cflags = ws.cflags;
     p.W = c.W; p.E = c.E; p.Er = c.Er; p.k = c.k; p.T = c.T; p.cap = c.cap;
     p.nvec = c.nvec;
+    p.nb = c.H / EP_QUANT_BLOCK;
     p.fused_wait = a.fused_wait ? 1 : 0;
     p.epoch = a.epoch;
     p.timeout_ns = c.timeout_ns;
@@ -356,12 +476,23 @@ cudaError_t launch_combine_wait(const Config &c, const Workspace &ws,
 
 cudaError_t launch_identity_expert(const Config &c, const Workspace &ws,
                                    char *y, int64_t y_stride, cudaStream_t st) {
+    IdentityParams a;
+    a.seg0 = ws.seg0;
+    a.seg_stride = ws.seg_stride;
+    a.off_out = ws.off_out;
+    a.off_scales = ws.off_scales;
+    a.off_w = ws.off_w;
+    a.off_idx = ws.off_idx;
+    a.totals = ws.group_base + (int64_t)c.Q * c.W;
+    a.y = y;
+    a.ysc = ws.seg0 + ws.off_comb_sc;
+    a.y_stride = y_stride;
+    a.W = c.W; a.E = c.E; a.Er = c.Er; a.k = c.k; a.H = c.H; a.cap = c.cap;
+    a.fp8 = c.fp8 ? 1 : 0;
+    a.yk = c.y_f32 ? kYF32 : (c.y_fp8 ? kYFp8 : kYBf16);
     const int64_t rows = (int64_t)c.W * c.cap;
     const int blocks = (int)((rows + 7) / 8);
-    identity_expert_kernel<<<blocks, 256, 0, st>>>(
-        ws.seg0, ws.seg_stride, ws.off_out, ws.off_scales, ws.off_w, ws.off_idx,
-        ws.group_base + (int64_t)c.Q * c.W, y, y_stride, c.W, c.E, c.Er, c.k,
-        c.H, c.cap, c.fp8 ? 1 : 0, c.y_f32 ? 1 : 0);
+    identity_expert_kernel<<<blocks, 256, 0, st>>>(a);
     return cudaGetLastError();
 }
 

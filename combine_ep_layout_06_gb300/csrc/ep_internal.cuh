@@ -43,7 +43,7 @@ struct Workspace {
     // rank-0 segment; rank r's copy is at + r * seg_stride bytes
     char *seg0;
     int64_t seg_stride;
-    int64_t off_out, off_scales, off_w, off_idx, off_src, off_comb;
+    int64_t off_out, off_scales, off_w, off_idx, off_src, off_comb, off_comb_sc;
     int64_t off_xg, off_xgs, off_gsrc, off_gw, off_yg, off_eslot;   // grouping
     size_t total_bytes;
 };
@@ -51,7 +51,8 @@ struct Workspace {
 struct Config {
     int W, E, Er, k, H, T, cap;
     bool fp8;
-    bool y_f32;  // combine reads fp32 expert rows (else bf16)
+    bool y_f32;  // combine reads fp32 expert rows
+    bool y_fp8;  // combine reads E4M3 expert rows + block scales (else bf16)
     int nch;     // chunks per source rank = ceil(T / kChunk)
     int G;       // W * nch
     int Q;       // layout groups = ceil(G / kGroup)
@@ -102,6 +103,7 @@ cudaError_t launch_combine_wait(const Config &c, const Workspace &ws,
 
 struct CombineArgs {
     const char *y;          // rank 0 rows; rank r at + r*y_stride
+    const char *ysc;        // FP8 payload: rank 0 block scales, same stride
     int64_t y_stride;
     const char *w_in;       // nullable
     int64_t w_stride;

@@ -31,12 +31,13 @@ class EpDispatchCombineConfig:
     early_notify: bool = False
     fused_recv: bool = False
     wait_timeout_ns: int = 0                 # 0 -> 1 s
-    combine_dtype: str = "bf16"              # expert rows combine reads: "bf16" | "fp32"
+    combine_dtype: str = "bf16"              # expert rows combine reads: "bf16" | "fp32" | "fp8_e4m3"
     max_grouped_rows_per_rank: int = 0       # standard-MoE grouping (0: off)
 
     def to_c(self) -> _lib.EpConfigC:
         dt = {"bf16": _lib.EP_DT_BF16, "fp8_e4m3": _lib.EP_DT_FP8_E4M3}
-        ct = {"bf16": _lib.EP_DT_BF16, "fp32": _lib.EP_DT_FP32}
+        ct = {"bf16": _lib.EP_DT_BF16, "fp32": _lib.EP_DT_FP32,
+              "fp8_e4m3": _lib.EP_DT_FP8_E4M3}
         if self.dispatch_dtype not in dt:
             raise ValueError(f"dispatch_dtype {self.dispatch_dtype!r}")
         if self.combine_dtype not in ct:
@@ -122,15 +123,22 @@ class EpDispatchCombineOp:
         self.combine_flags = view(o.combine_flags, torch.int32, (W, W), (W, 1))
         p = ctypes.c_void_p()
         s = ctypes.c_int64()
-        y32 = c.combine_dtype == "fp32"
-        check(self.L.ep_get_combine_input_buffer(
-                  self.h, _lib.EP_DT_FP32 if y32 else _lib.EP_DT_BF16,
-                  ctypes.byref(p), ctypes.byref(s)),
+        ydt = {"bf16": (_lib.EP_DT_BF16, torch.bfloat16, 2),
+               "fp32": (_lib.EP_DT_FP32, torch.float32, 4),
+               "fp8_e4m3": (_lib.EP_DT_FP8_E4M3, torch.uint8, 1)}[c.combine_dtype]
+        check(self.L.ep_get_combine_input_buffer(self.h, ydt[0], ctypes.byref(p),
+                                                 ctypes.byref(s)),
               "ep_get_combine_input_buffer")
-        self.y_dtype = torch.float32 if y32 else torch.bfloat16
-        esz = 4 if y32 else 2
+        self.y_dtype = ydt[1]
         self.combine_input = view(p.value, self.y_dtype, (W, cap, H),
-                                  (s.value // esz, H, 1))
+                                  (s.value // ydt[2], H, 1))
+        self.combine_input_scales = None
+        if c.combine_dtype == "fp8_e4m3":
+            ps = ctypes.c_void_p()
+            check(self.L.ep_get_combine_input_scales(self.h, ctypes.byref(ps), ctypes.byref(s)),
+                  "ep_get_combine_input_scales")
+            self.combine_input_scales = view(ps.value, torch.float32, (W, cap, nb),
+                                             (s.value // 4, nb, 1))
         self.rank_stride_bytes = rs
         if c.max_grouped_rows_per_rank > 0:
             m = _lib.EpMoeOutC()
@@ -237,6 +245,8 @@ class EpDispatchCombineOp:
             out_weights = torch.empty((W, T, k), dtype=torch.float32,
                                       device=self.device)
         ys = 0
+        if input is not None and self.config.combine_dtype == "fp8_e4m3":
+            raise ValueError("an FP8 combine payload is read from the registered buffer")
         if input is not None:
             if input.dtype != self.y_dtype or input.dim() != 3 or \
                     input.shape[0] != W or input.shape[2] != H or input.stride(2) != 1 \

@@ -120,8 +120,11 @@ typedef struct {
                                          itself, one warp per CTA, then a CTA
                                          barrier releases the gather warps */
     int32_t combine_dtype;            /* element type of the expert rows that
-                                         combine reads: EP_DT_BF16 (0) or
-                                         EP_DT_FP32; the output is bf16 */
+                                         combine reads: EP_DT_BF16 (0),
+                                         EP_DT_FP32, or EP_DT_FP8_E4M3 (codes
+                                         + one fp32 scale per 128 elements,
+                                         registered buffer only; H % 128 == 0);
+                                         the output is bf16 */
     int64_t wait_timeout_ns;          /* bound of every device wait; 0 = 1 s */
     int32_t max_grouped_rows_per_rank;/* rows of the standard-MoE grouped
                                          buffers per rank (0: no grouping);
@@ -222,6 +225,14 @@ ep_status_t ep_get_combine_input_buffer(const ep_handle_t *h, int32_t dtype,
                                         void **d_ptr,
                                         int64_t *rank_stride_bytes);
 
+/* FP8 combine payload (combine_dtype == EP_DT_FP8_E4M3): the block scales
+ * of the registered combine buffer, rank r's [cap][H/128] fp32 rows at
+ * *d_ptr + r * *rank_stride_bytes.  Combine dequantises each element as
+ * fl32(e4m3_value(q) * scale) before its ordered fp32 sum.  NOT_FOUND for
+ * other combine dtypes. */
+ep_status_t ep_get_combine_input_scales(const ep_handle_t *h, float **d_ptr,
+                                        int64_t *rank_stride_bytes);
+
 /* Send phase of combine (expert side): records the completion of the
  * expert's work on `stream` and (early_notify) posts combine ready flags. */
 ep_status_t ep_combine_send(ep_handle_t *h, void *stream);
@@ -296,7 +307,9 @@ ep_status_t ep_get_error(ep_handle_t *h, uint32_t *mask, void *stream);
  * benchmark's correctness check ("Validation before tuning").  For each
  * received row p < min(recv_count[r], cap) of every rank r:
  * alpha = ordered fp32 sum of the row's weights whose expert lives on r,
- * y_r[p][h] = bf16_rne(fl32(v_h * alpha)) (fp32 rows: fl32(v_h * alpha)),
+ * y_r[p][h] = bf16_rne(fl32(v_h * alpha)) (fp32 rows: fl32(v_h * alpha);
+ * FP8 payload: those fp32 products quantised per 128-element block with the
+ * dispatch formula),
  * v = the bf16 payload, or fl32(e4m3_value(q) * scale) for FP8.  d_y as in
  * ep_combine_recv. */
 ep_status_t ep_test_identity_expert(ep_handle_t *h, void *d_y,

@@ -74,7 +74,7 @@ def test_workspace_size_and_config_validation(L):
            dict(topk=0), dict(topk=33), dict(hidden=7170), dict(hidden=0),
            dict(max_tokens_per_rank=0), dict(dispatch_dtype=1, hidden=7168 + 8),
            dict(dispatch_dtype=7), dict(max_recv_tokens_per_rank=-1),
-           dict(fused_recv=1, early_notify=0), dict(combine_dtype=1),
+           dict(fused_recv=1, early_notify=0), dict(combine_dtype=1, hidden=7176),
            dict(combine_dtype=5)]
     for b in bad:
         assert _size(L, **b)[0] == 3, b      # EP_ERR_INVALID_ARGS
