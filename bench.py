@@ -59,6 +59,8 @@ def parse():
                     help="FP8 workloads: dispatch a pre-quantised payload (codes + scales)")
     ap.add_argument("--combine-dtype", choices=["bf16", "fp32", "fp8_e4m3"], default="bf16",
                     help="element type of the expert rows combine reads")
+    ap.add_argument("--combine-mode", choices=["gather", "scatter"], default="gather",
+                    help="gather combine, or scatter combine through a staging area")
     ap.add_argument("--moe-group", type=int, default=0, metavar="GCAP",
                     help="also time the standard-MoE grouping / un-grouping with "
                          "GCAP grouped rows per rank (reported beside the step)")
@@ -68,7 +70,7 @@ def parse():
 # ------------------------------------------------------------- bookkeeping
 
 def algorithmic_bytes(wl, P, N, fp8, with_weights=True, fp8_input=False,
-                      y_bytes=2):
+                      y_bytes=2, scatter=False):
     """Bytes the method must move (each counted once).
     dispatch: read N*(H*b_in + s_in + 8k) [row once (+ its scales) + ids +
               weights]; write P*(H*b + s_b + 8k + 4) [row, scales, weights,
@@ -80,7 +82,12 @@ def algorithmic_bytes(wl, P, N, fp8, with_weights=True, fp8_input=False,
     d_read = N * ((H + s_b) if fp8_input else H * 2) + N * 8 * k
     d_write = P * (H * b_out + s_b + 8 * k + 4)
     c_read = P * H * y_bytes + (P * 4 * k if with_weights else 0)
-    c_write = N * H * 2 + (N * 4 * k if with_weights else 0)
+    if scatter:   # rows pushed to the staging area, then read back
+        c_read += P * H * 2
+        c_write_extra = P * H * 2
+    else:
+        c_write_extra = 0
+    c_write = N * H * 2 + (N * 4 * k if with_weights else 0) + c_write_extra
     return dict(dispatch=d_read + d_write, combine=c_read + c_write,
                 dispatch_read=d_read, dispatch_write=d_write,
                 combine_read=c_read, combine_write=c_write)
@@ -215,7 +222,8 @@ def run_ours(args, rank, world, local_rank):
                                   max_recv_tokens_per_rank=args.cap,
                                   dispatch_dtype="fp8_e4m3" if wl.fp8 else "bf16",
                                   combine_dtype=args.combine_dtype,
-                                  max_grouped_rows_per_rank=args.moe_group)
+                                  max_grouped_rows_per_rank=args.moe_group,
+                                  combine_mode=args.combine_mode)
     op = EpDispatchCombineOp(cfg, device=dev)
     x = torch.from_numpy(inp.x_bits.view(np.int16)).to(dev).view(torch.bfloat16)
     xsc = None
@@ -307,7 +315,8 @@ def run_ours(args, rank, world, local_rank):
     value = world * N / (ms_per_step / 1e3)
 
     ab = algorithmic_bytes(wl, P, N, wl.fp8, fp8_input=args.fp8_input,
-                           y_bytes={"fp32": 4, "bf16": 2, "fp8_e4m3": 1 + 4 / 128}[args.combine_dtype])
+                           y_bytes={"fp32": 4, "bf16": 2, "fp8_e4m3": 1 + 4 / 128}[args.combine_dtype],
+                           scatter=args.combine_mode == "scatter")
     step_bytes = ab["dispatch"] + ab["combine"]
     peak, peak_kind = measured_peak()
     d_ms, c_ms = float(dis.mean()), float(com.mean())

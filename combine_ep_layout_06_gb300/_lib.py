@@ -49,7 +49,7 @@ class EpConfigC(ctypes.Structure):
         ("combine_dtype", ctypes.c_int32),
         ("wait_timeout_ns", ctypes.c_int64),
         ("max_grouped_rows_per_rank", ctypes.c_int32),
-        ("reserved1", ctypes.c_int32),
+        ("combine_mode", ctypes.c_int32),
     ]
 
 
@@ -85,7 +85,8 @@ class EpDispatchOutC(ctypes.Structure):
         ("dispatch_epoch", ctypes.c_uint32),
         ("combine_epoch", ctypes.c_uint32),
         ("cap", ctypes.c_int32),
-        ("reserved0", ctypes.c_int32),
+        ("max_dest", ctypes.c_int32),
+        ("combine_stage", ctypes.c_void_p),
     ]
 
 

@@ -68,6 +68,11 @@ ep_status_t make_config(const ep_config_t *in, Config *c) {
         (int64_t)in->max_grouped_rows_per_rank > (int64_t)1 << 30)
         return EP_ERR_INVALID_ARGS;
     c->gcap = in->max_grouped_rows_per_rank;
+    if (in->combine_mode != EP_COMBINE_GATHER && in->combine_mode != EP_COMBINE_SCATTER)
+        return EP_ERR_INVALID_ARGS;
+    c->scatter = in->combine_mode == EP_COMBINE_SCATTER;
+    if (c->scatter && (c->y_f32 || c->y_fp8)) return EP_ERR_INVALID_ARGS;
+    c->maxd = W < k ? W : k;
     c->nrc = (c->cap + kChunk - 1) / kChunk;
     return EP_SUCCESS;
 }
@@ -118,6 +123,7 @@ void plan_workspace(const Config &c, char *base, Workspace *ws) {
     ws->moe_base = reinterpret_cast<int32_t *>(take(W * nrc * Er * 4));
     ws->moe_count = reinterpret_cast<int32_t *>(take(moe ? W * Er * 4 : 0));
     ws->moe_offset = reinterpret_cast<int32_t *>(take(moe ? W * Er * 4 : 0));
+    ws->stage = take(c.scatter ? W * T * (size_t)c.maxd * c.H * 2 : 0);
     // one rank segment
     const size_t cap = c.cap, H = c.H, k = c.k;
     size_t so = 0;
@@ -366,7 +372,8 @@ ep_status_t ep_dispatch_outputs(const ep_handle_t *h, ep_dispatch_out_t *o) {
     o->dispatch_epoch = h->dispatch_epoch;
     o->combine_epoch = h->combine_epoch;
     o->cap = h->cfg.cap;
-    o->reserved0 = 0;
+    o->max_dest = h->cfg.maxd;
+    o->combine_stage = h->cfg.scatter ? ws.stage : nullptr;
     return EP_SUCCESS;
 }
 
@@ -393,6 +400,10 @@ ep_status_t ep_combine_send(ep_handle_t *h, void *stream) {
     if (!h) return EP_ERR_INVALID_ARGS;
     if (!h->layout_valid || h->combine_pending) return EP_ERR_BAD_STATE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (h->cfg.scatter) {
+        const ep_status_t s = gpu(h, launch_scatter_send(h->cfg, h->ws, st), "scatter_send");
+        if (s != EP_SUCCESS) return s;
+    }
     if (h->cfg.early_notify) {
         ++h->combine_epoch;
         const ep_status_t s = gpu(h, launch_combine_notify(h->cfg, h->ws, h->combine_epoch, st),
@@ -415,7 +426,9 @@ static ep_status_t combine_args(ep_handle_t *h, const void *d_y, int64_t y_strid
     if ((d_w_in == nullptr) != (d_out_w == nullptr)) return EP_ERR_INVALID_ARGS;
     const int64_t row_bytes = (int64_t)c.cap * c.H * (c.y_f32 ? 4 : 2);
     a->ysc = h->ws.seg0 + h->ws.off_comb_sc;
-    if (d_y && c.y_fp8) return EP_ERR_INVALID_ARGS;   // FP8 payload: registered buffer only
+    a->stage = c.scatter ? h->ws.stage : nullptr;
+    // FP8 payload and scatter mode: the registered buffer only
+    if (d_y && (c.y_fp8 || c.scatter)) return EP_ERR_INVALID_ARGS;
     if (d_y) {
         if (y_stride == 0) y_stride = row_bytes;
         if (!aligned(d_y, 16) || y_stride % 16 != 0 || y_stride < row_bytes)
@@ -479,6 +492,10 @@ ep_status_t ep_combine(ep_handle_t *h, const void *d_y, int64_t y_rank_stride_by
     if (s != EP_SUCCESS) return s;
     if (!h->layout_valid || h->combine_pending) return EP_ERR_BAD_STATE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (h->cfg.scatter) {
+        s = gpu(h, launch_scatter_send(h->cfg, h->ws, st), "scatter_send");
+        if (s != EP_SUCCESS) return s;
+    }
     if (h->cfg.early_notify) {
         ++h->combine_epoch;
         a.epoch = h->combine_epoch;

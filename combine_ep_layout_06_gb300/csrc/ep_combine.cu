@@ -45,6 +45,8 @@ constexpr int kYBf16 = 0, kYF32 = 1, kYFp8 = 2;
 struct CombineParams {
     const char *y;
     const char *ysc;          // FP8 rows: block scales, same rank stride as y
+    const char *stage;        // scatter combine: staged rows [W*T][maxd][H], or null
+    int maxd;
     int64_t y_stride;
     const char *w_in;
     int64_t w_stride;
@@ -222,7 +224,8 @@ combine_kernel(const CombineParams p) {
                 const int r = __ffs(mm) - 1;
                 mm &= mm - 1u;
                 const int slot = __shfl_sync(0xffffffffu, pr, r);
-                rows[j] = p.y + (int64_t)r * p.y_stride + (int64_t)slot * p.nvec * VB;
+                rows[j] = p.stage ? p.stage + (tok * p.maxd + j) * (int64_t)p.nvec * VB
+                                  : p.y + (int64_t)r * p.y_stride + (int64_t)slot * p.nvec * VB;
                 if constexpr (YK == kYFp8)
                     srows[j] = p.ysc + (int64_t)r * p.y_stride + (int64_t)slot * p.nb * 4;
                 nd = j + 1;
@@ -285,6 +288,37 @@ __global__ void flags_wait_kernel(const uint32_t *flags, uint32_t *words,
     const int i = threadIdx.x;
     if (i < n && !wait_flag_eq(flags + i, epoch, timeout_ns))
         set_error(words, EP_DEVERR_TIMEOUT);
+}
+
+// Scatter combine, expert side: warp per received row; the row's expert
+// output goes to stage[s][t][d], d = the number of the token's destinations
+// below this rank, so the source side finds a token's rows contiguous and in
+// ascending rank order.
+__global__ void __launch_bounds__(256)
+scatter_send_kernel(const char *seg0, int64_t seg_stride, int64_t off_src, int64_t off_comb,
+                    const int32_t *totals, const int32_t *pos, char *stage,
+                    int W, int T, int cap, int maxd, int nvec) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int r = (int)(gw / cap);
+    const int row = (int)(gw - (int64_t)r * cap);
+    if (r >= W || row >= min(totals[r], cap)) return;
+    const char *seg = seg0 + (int64_t)r * seg_stride;
+    const int64_t tok = reinterpret_cast<const int32_t *>(seg + off_src)[row];   // s*T + t
+    const int pr = lane < W ? pos[tok * W + lane] : -1;
+    const uint32_t m = __ballot_sync(0xffffffffu, pr >= 0 && pr < cap);
+    const int d = __popc(m & ((1u << r) - 1u));
+    const uint4 *src = reinterpret_cast<const uint4 *>(seg + off_comb) + (int64_t)row * nvec;
+    uint4 *dst = reinterpret_cast<uint4 *>(stage) + (tok * maxd + d) * (int64_t)nvec;
+    for (int v0 = lane; v0 < nvec; v0 += 32 * 4) {
+        uint4 b[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (v0 + 32 * u < nvec) b[u] = ld_stream16(src + v0 + 32 * u);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (v0 + 32 * u < nvec) st_stream16(dst + v0 + 32 * u, b[u]);
+    }
 }
 
 // 8 fp32 values -> 8 E4M3 codes given the block scale.
@@ -435,6 +469,8 @@ cudaError_t launch_combine(const Config &c, const Workspace &ws,
     CombineParams p;
     p.y = a.y;
     p.ysc = a.ysc;
+    p.stage = a.stage;
+    p.maxd = c.maxd;
     p.y_stride = a.y_stride;
     p.w_in = a.w_in;
     p.w_stride = a.w_stride;
@@ -471,6 +507,14 @@ cudaError_t launch_combine_wait(const Config &c, const Workspace &ws,
     const int n = c.W * c.W;
     flags_wait_kernel<<<1, ((n + 31) / 32) * 32, 0, st>>>(ws.cflags, ws.words, n,
                                                           epoch, c.timeout_ns);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scatter_send(const Config &c, const Workspace &ws, cudaStream_t st) {
+    const int64_t rows = (int64_t)c.W * c.cap;
+    scatter_send_kernel<<<(int)((rows + 7) / 8), 256, 0, st>>>(
+        ws.seg0, ws.seg_stride, ws.off_src, ws.off_comb, ws.group_base + (int64_t)c.Q * c.W,
+        ws.pos, ws.stage, c.W, c.T, c.cap, c.maxd, c.nvec);
     return cudaGetLastError();
 }
 

@@ -40,6 +40,7 @@ struct Workspace {
     int32_t *moe_base;     // [W][nrc][Er] exclusive prefix over chunks
     int32_t *moe_count;    // [W][Er]
     int32_t *moe_offset;   // [W][Er]
+    char *stage;           // scatter combine: [W][T][maxd][H] bf16 staged rows
     // rank-0 segment; rank r's copy is at + r * seg_stride bytes
     char *seg0;
     int64_t seg_stride;
@@ -57,6 +58,8 @@ struct Config {
     int G;       // W * nch
     int Q;       // layout groups = ceil(G / kGroup)
     int gcap;    // grouped rows per rank (0: no standard-MoE grouping)
+    bool scatter;  // scatter combine (staging on the source side)
+    int maxd;    // min(W, k): destinations per token at most
     int nrc;     // 32-row chunks of received rows per rank = ceil(cap / 32)
     int nvec;    // 16-byte vectors per bf16 row = H / 8
     int nb;      // FP8 blocks per row = H / 128 (0 for bf16)
@@ -104,6 +107,7 @@ cudaError_t launch_combine_wait(const Config &c, const Workspace &ws,
 struct CombineArgs {
     const char *y;          // rank 0 rows; rank r at + r*y_stride
     const char *ysc;        // FP8 payload: rank 0 block scales, same stride
+    const char *stage;      // scatter combine: staged rows instead of y
     int64_t y_stride;
     const char *w_in;       // nullable
     int64_t w_stride;
@@ -116,6 +120,10 @@ struct CombineArgs {
 };
 cudaError_t launch_combine(const Config &c, const Workspace &ws,
                            const CombineArgs &a, cudaStream_t st);
+
+// Scatter combine, send side: every received row's expert output to its
+// token's staging slot.
+cudaError_t launch_scatter_send(const Config &c, const Workspace &ws, cudaStream_t st);
 
 cudaError_t launch_moe_group(const Config &c, const Workspace &ws, cudaStream_t st);
 cudaError_t launch_moe_ungroup(const Config &c, const Workspace &ws, const char *yg,

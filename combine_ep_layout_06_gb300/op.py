@@ -33,6 +33,7 @@ class EpDispatchCombineConfig:
     wait_timeout_ns: int = 0                 # 0 -> 1 s
     combine_dtype: str = "bf16"              # expert rows combine reads: "bf16" | "fp32" | "fp8_e4m3"
     max_grouped_rows_per_rank: int = 0       # standard-MoE grouping (0: off)
+    combine_mode: str = "gather"             # "gather" | "scatter"
 
     def to_c(self) -> _lib.EpConfigC:
         dt = {"bf16": _lib.EP_DT_BF16, "fp8_e4m3": _lib.EP_DT_FP8_E4M3}
@@ -47,7 +48,8 @@ class EpDispatchCombineConfig:
             self.max_tokens_per_rank, self.max_recv_tokens_per_rank,
             dt[self.dispatch_dtype], int(self.early_notify),
             int(self.fused_recv), ct[self.combine_dtype],
-            int(self.wait_timeout_ns), int(self.max_grouped_rows_per_rank), 0)
+            int(self.wait_timeout_ns), int(self.max_grouped_rows_per_rank),
+            {"gather": 0, "scatter": 1}[self.combine_mode])
 
 
 def workspace_size(cfg: EpDispatchCombineConfig) -> int:
@@ -119,6 +121,11 @@ class EpDispatchCombineOp:
         self.recv_count = view(o.recv_count, torch.int32, (W,), (1,))
         self.send_counts = view(o.send_counts, torch.int32, (W, W), (W, 1))
         self.pos = view(o.pos, torch.int32, (W, T, W), (T * W, W, 1))
+        self.combine_stage = None
+        if o.combine_stage:
+            md = o.max_dest
+            self.combine_stage = view(o.combine_stage, torch.bfloat16, (W, T, md, H),
+                                      (T * md * H, md * H, H, 1))
         self.dispatch_flags = view(o.dispatch_flags, torch.int32, (W, W), (W, 1))
         self.combine_flags = view(o.combine_flags, torch.int32, (W, W), (W, 1))
         p = ctypes.c_void_p()

@@ -129,8 +129,20 @@ typedef struct {
     int32_t max_grouped_rows_per_rank;/* rows of the standard-MoE grouped
                                          buffers per rank (0: no grouping);
                                          cap * k is the exact worst case */
-    int32_t reserved1;
+    int32_t combine_mode;             /* EP_COMBINE_GATHER (0): combine_recv
+                                         gathers the expert rows from the
+                                         destination segments.
+                                         EP_COMBINE_SCATTER: combine_send pushes
+                                         every received row's expert output to a
+                                         per-token staging area on the source
+                                         side (slot = the rank's order among the
+                                         token's destinations) and combine_recv
+                                         reduces the staged rows; bf16 rows from
+                                         the registered buffer only */
 } ep_config_t;
+
+#define EP_COMBINE_GATHER 0
+#define EP_COMBINE_SCATTER 1
 
 typedef struct ep_handle ep_handle_t;
 
@@ -153,7 +165,8 @@ typedef struct {
     uint32_t  dispatch_epoch; /* value the flags carry for the last send */
     uint32_t  combine_epoch;
     int32_t   cap;
-    int32_t   reserved0;
+    int32_t   max_dest;       /* min(W, k) */
+    void     *combine_stage;  /* scatter combine: [W][T][max_dest][H] bf16, or NULL */
 } ep_dispatch_out_t;
 
 const char *ep_status_str(ep_status_t s);
