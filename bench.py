@@ -196,6 +196,24 @@ class ClockSampler:
                 "window": note}
 
 
+# ------------------------------------------------------------ replicas
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's time: every rank times its own replica and the job
+    is done when the last one is (all_reduce MAX; a no-op for one rank)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_replica: int, world: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: all replicas' tokens over the slowest step time."""
+    return world * tokens_per_replica / (ms_per_step / 1e3)
+
+
 # ------------------------------------------------------------ our path
 
 def run_ours(args, rank, world, local_rank):
@@ -307,12 +325,9 @@ def run_ours(args, rank, world, local_rank):
         sampler.stop()
     st, mask = op.get_error(stream)
 
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * N / (ms_per_step / 1e3)
+    value = job_throughput(N, world, ms_per_step)
 
     ab = algorithmic_bytes(wl, P, N, wl.fp8, fp8_input=args.fp8_input,
                            y_bytes={"fp32": 4, "bf16": 2, "fp8_e4m3": 1 + 4 / 128}[args.combine_dtype],
@@ -363,14 +378,11 @@ def run_ours(args, rank, world, local_rank):
             e1.record(stream)
         e1.synchronize()
         e_ms = e0.elapsed_time(e1) / args.e2e_steps
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e_ms, world, dev)
         h2d = hx.numel() * hx.element_size() + hw.numel() * 4 + hi.numel() * 4 + \
             (0 if hsc is None else hsc.numel() * 4)
         d2h = hout.numel() * 2
-        e2e = {"value": world * N / (e_ms / 1e3), "unit": "tokens/s",
+        e2e = {"value": job_throughput(N, world, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e_ms}
 

@@ -182,7 +182,7 @@ __device__ __forceinline__ void add_vec(float acc[8], const RowVec &r) {
     }
 }
 
-template <int MAXD, int U, bool COHERENT, int YK>
+template <int MAXD, int U, bool COHERENT, int YK, bool STAGED>
 __global__ void __launch_bounds__(kCombineThreads, EP_COMBINE_MIN_BLOCKS)
 combine_kernel(const CombineParams p) {
     // bytes of one column vector of an expert row: bf16 16, fp32 32, FP8 8
@@ -224,8 +224,10 @@ combine_kernel(const CombineParams p) {
                 const int r = __ffs(mm) - 1;
                 mm &= mm - 1u;
                 const int slot = __shfl_sync(0xffffffffu, pr, r);
-                rows[j] = p.stage ? p.stage + (tok * p.maxd + j) * (int64_t)p.nvec * VB
-                                  : p.y + (int64_t)r * p.y_stride + (int64_t)slot * p.nvec * VB;
+                if constexpr (STAGED)   // scatter combine: the token's staged rows
+                    rows[j] = p.stage + (tok * p.maxd + j) * (int64_t)p.nvec * VB;
+                else
+                    rows[j] = p.y + (int64_t)r * p.y_stride + (int64_t)slot * p.nvec * VB;
                 if constexpr (YK == kYFp8)
                     srows[j] = p.ysc + (int64_t)r * p.y_stride + (int64_t)slot * p.nb * 4;
                 nd = j + 1;
@@ -444,7 +446,13 @@ cudaError_t launch_combine_t(const Config &c, const CombineParams &p,
                              cudaStream_t st) {
     const int64_t tokens = (int64_t)c.W * c.T;
     const int blocks = (int)((tokens + kCombineWarps - 1) / kCombineWarps);
-    combine_kernel<MAXD, U, COH, YK><<<blocks, kCombineThreads, 0, st>>>(p);
+    if constexpr (YK == kYBf16) {
+        if (p.stage) {
+            combine_kernel<MAXD, U, COH, YK, true><<<blocks, kCombineThreads, 0, st>>>(p);
+            return cudaGetLastError();
+        }
+    }
+    combine_kernel<MAXD, U, COH, YK, false><<<blocks, kCombineThreads, 0, st>>>(p);
     return cudaGetLastError();
 }
 
