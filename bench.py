@@ -342,49 +342,78 @@ def run_ours(args, rank, world, local_rank):
              else ("dispatch_kernel" if wl.fp8 and not args.fp8_input
                    else "dispatch_bulk_kernel"))
 
-    # end to end: pinned host inputs -> device, path, combined output -> host
+    # end to end: pinned host inputs -> device, path, combined output -> host.
+    # Every step copies its own inputs in and its combined output out; the
+    # copies of neighbouring steps overlap the compute through three streams
+    # (H2D of step i+1 | dispatch + combine of step i | D2H of step i-1) and
+    # double-buffered device inputs and outputs.
     e2e = None
     if args.e2e_steps > 0:
         hx = x.cpu().pin_memory()
         hsc = None if xsc is None else xsc.cpu().pin_memory()
         hw = torch.from_numpy(inp.weights).pin_memory()
         hi = torch.from_numpy(inp.indices).pin_memory()
-        hout = torch.empty((W, T, H), dtype=torch.bfloat16).pin_memory()
-        dx, dw, di = torch.empty_like(x), torch.empty_like(w), torch.empty_like(idx)
-        dsc = None if xsc is None else torch.empty_like(xsc)
+        hout = [torch.empty((W, T, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        dx = [torch.empty_like(x) for _ in range(2)]
+        dw = [torch.empty_like(w) for _ in range(2)]
+        di = [torch.empty_like(idx) for _ in range(2)]
+        dsc = [None if xsc is None else torch.empty_like(xsc) for _ in range(2)]
+        dout = [torch.empty_like(out) for _ in range(2)]
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_comp = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        for b in range(2):      # all buffers free at the start
+            ev_comp[b].record(stream)
+            ev_out[b].record(s_out)
 
-        def e2e_step():
-            dx.copy_(hx, non_blocking=True)
-            if dsc is not None:
-                dsc.copy_(hsc, non_blocking=True)
-            dw.copy_(hw, non_blocking=True)
-            di.copy_(hi, non_blocking=True)
-            op.dispatch(dx, dw, dsc, di, num_tokens=nt, stream=stream)
-            op.combine(weights=op.out_w, out=out, out_weights=out_w, stream=stream)
-            hout.copy_(out, non_blocking=True)
+        def e2e_step(i):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_comp[b])            # step i-2 has consumed slot b
+                dx[b].copy_(hx, non_blocking=True)
+                if dsc[b] is not None:
+                    dsc[b].copy_(hsc, non_blocking=True)
+                dw[b].copy_(hw, non_blocking=True)
+                di[b].copy_(hi, non_blocking=True)
+                ev_in[b].record(s_in)
+            stream.wait_event(ev_in[b])
+            stream.wait_event(ev_out[b])               # D2H of step i-2 has read dout[b]
+            op.dispatch(dx[b], dw[b], dsc[b], di[b], num_tokens=nt, stream=stream)
+            op.combine(weights=op.out_w, out=dout[b], out_weights=out_w, stream=stream)
+            ev_comp[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[b])
+                hout[b].copy_(dout[b], non_blocking=True)
+                ev_out[b].record(s_out)
 
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                e2e_step()
+        for i in range(3):
+            e2e_step(i)
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(args.e2e_steps):
-                e2e_step()
-            e1.record(stream)
+        e0.record(s_in)
+        stream.wait_event(e0)
+        s_out.wait_event(e0)
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        s_out.wait_stream(stream)
+        s_out.wait_stream(s_in)
+        e1.record(s_out)
         e1.synchronize()
         e_ms = e0.elapsed_time(e1) / args.e2e_steps
         e_ms = max_over_ranks(e_ms, world, dev)
         h2d = hx.numel() * hx.element_size() + hw.numel() * 4 + hi.numel() * 4 + \
             (0 if hsc is None else hsc.numel() * 4)
-        d2h = hout.numel() * 2
+        d2h = hout[0].numel() * 2
+        # the copied-back output equals the device result of the same inputs
+        e2e_ok = bool(torch.equal(hout[(args.e2e_steps - 1) % 2].to(dev), out))
         e2e = {"value": job_throughput(N, world, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": e_ms}
+               "ms_per_step": e_ms, "pipelined": "H2D / compute / D2H on three streams",
+               "output_check": "pass" if e2e_ok else "FAIL"}
 
     moe = None
     if args.moe_group:

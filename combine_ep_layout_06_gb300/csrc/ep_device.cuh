@@ -9,12 +9,26 @@
 
 namespace ep {
 
+#ifndef EP_LD_L2_PREFETCH
+#define EP_LD_L2_PREFETCH 0     // 0, 128 or 256: L2 prefetch size on streaming reads
+#endif
+
 // Streaming read of data used once (not allocated in L1).
 __device__ __forceinline__ uint4 ld_stream16(const void *p) {
     uint4 v;
+#if EP_LD_L2_PREFETCH == 256
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+#elif EP_LD_L2_PREFETCH == 128
+    asm volatile("ld.global.nc.L1::no_allocate.L2::128B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+#else
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
+#endif
     return v;
 }
 
