@@ -521,34 +521,39 @@ constexpr int kBulkStages =
 template <int STAGES, int TPC>
 cudaError_t launch_dispatch_bulk(const Config &c, const DispatchParams &p,
                                  cudaStream_t st) {
-    static size_t configured = 0;       // per instantiation
-    static long share = -1;             // smem per CTA at the capped residency
+    // Function attributes are per device: cache the opted-in size and the
+    // capped-residency share per device.
+    constexpr int kMaxDevices = 64;
+    static size_t configured[kMaxDevices] = {};
+    static long share[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     const size_t row = (size_t)p.row_bytes;
     size_t dyn = (size_t)STAGES * row;
     const size_t per_cta = (size_t)TPC * (size_t)(c.W < c.k ? c.W : c.k) * row;
     if (EP_DISPATCH_BULK_CTAS_PER_SM > 0 && per_cta >= 64 * 1024) {
-        if (share < 0) {
-            int dev = 0, per_sm = 0, reserved = 0;
+        if (share[dev] == 0) {
+            int per_sm = 0, reserved = 0;
             cudaFuncAttributes fa;
-            if (cudaGetDevice(&dev) != cudaSuccess ||
-                cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
-                                       dev) != cudaSuccess ||
-                cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock,
-                                       dev) != cudaSuccess ||
-                cudaFuncGetAttributes(&fa, dispatch_bulk_kernel<STAGES, TPC>) != cudaSuccess)
-                return cudaGetLastError();
+            if ((e = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                            dev)) != cudaSuccess ||
+                (e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock,
+                                            dev)) != cudaSuccess ||
+                (e = cudaFuncGetAttributes(&fa, dispatch_bulk_kernel<STAGES, TPC>)) != cudaSuccess)
+                return e;
             const long v = (long)per_sm / EP_DISPATCH_BULK_CTAS_PER_SM - reserved -
                            (long)fa.sharedSizeBytes;
-            share = v > 0 ? (v & ~127L) : 0;
+            share[dev] = v > 0 ? (v & ~127L) : -1;
         }
-        if ((size_t)share > dyn) dyn = (size_t)share;
+        if (share[dev] > 0 && (size_t)share[dev] > dyn) dyn = (size_t)share[dev];
     }
-    if (dyn > configured) {             // opt in to the dynamic size
-        const cudaError_t e = cudaFuncSetAttribute(
-            dispatch_bulk_kernel<STAGES, TPC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-            (int)dyn);
+    if (dyn > configured[dev]) {        // opt in to the dynamic size
+        e = cudaFuncSetAttribute(dispatch_bulk_kernel<STAGES, TPC>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
         if (e != cudaSuccess) return e;
-        configured = dyn;
+        configured[dev] = dyn;
     }
     dispatch_bulk_kernel<STAGES, TPC><<<c.G * (kChunk / TPC), kDispatchThreads, dyn, st>>>(p);
     return cudaGetLastError();

@@ -144,6 +144,7 @@ typedef struct {
 #define EP_COMBINE_GATHER 0
 #define EP_COMBINE_SCATTER 1
 
+/* A handle is not thread-safe: drive it from one host thread at a time. */
 typedef struct ep_handle ep_handle_t;
 
 /* Device views of the dispatch results (valid until the next dispatch,
