@@ -1,0 +1,49 @@
+"""Every FP8 code and block scale of the fused quantising dispatch over
+16384 rows of H=7168 (117 M elements) against the oracle's E4M3 encoder,
+plus rows built to hit exact round-to-nearest ties (block amax 448, so the
+scale is exactly 1 and the midpoints between E4M3 values are bf16-exact),
+rows of values that land in E4M3's subnormal range, and signed zeros."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_ep_layout_06_gb300 import inputs as gen
+from gpu_helpers import make_op, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _tie_row(H, sign):
+    mids = [(1 + m / 8 + 1 / 16) * 2.0 ** e for e in range(-6, 8) for m in range(8)]
+    row = np.zeros(H, np.float32)
+    for b in range(H // 128):
+        blk = np.array([448.0] + [sign * v for v in mids], np.float32)
+        row[b * 128:b * 128 + blk.size] = blk[:128]
+    return row
+
+
+def test_fused_fp8_codes_match_the_oracle_everywhere():
+    H = 7168
+    wl = gen.Workload("codes", 2, 2, 1, 8192, H, fp8=True)
+    inp = gen.make_inputs(wl)
+    xf = np.zeros((4, H), np.float32)
+    xf[0] = _tie_row(H, 1.0)
+    xf[1] = _tie_row(H, -1.0)
+    xf[2] = np.linspace(-1.0, 1.0, H).astype(np.float32) * 2.0 ** -14
+    xf[2, ::128] = 1.0                         # amax 1: most values E4M3-subnormal
+    xf[3] = -0.0
+    xf[3, 7] = 3.0
+    inp.x_bits[0, :4] = (xf.view(np.uint32) >> 16).astype(np.uint16)
+    op = make_op(wl)
+    x, w, idx = to_device(inp)
+    op.dispatch(x, w, None, idx)
+    torch.cuda.synchronize()
+    rc = op.recv_count.cpu().numpy()
+    for r in range(2):
+        n = int(rc[r])
+        src = op.src_pos[r, :n].cpu().numpy()
+        s_, t_ = np.divmod(src, wl.max_tokens_per_rank)
+        q, sc = oracle.quant_rows(inp.x_bits[s_, t_])
+        assert np.array_equal(op.out[r, :n].cpu().numpy(), q), r
+        assert np.array_equal(op.out_scales[r, :n].cpu().numpy().view(np.uint32), sc.view(np.uint32))
