@@ -12,7 +12,9 @@ the registered combine buffer, filled once before timing by the identity
 expert of the correctness check.
 
 Prints ONE JSON line (rank 0).  `value` = tokens/s over all ranks (tokens =
-W*T per replica per step), device-timed with CUDA events; `e2e` = the same
+W*T per replica per step), device-timed with CUDA events around K replays
+of a CUDA graph of the step (`--eager`: K host-launched steps); the
+per-kernel times and the roofline come from eager steps; `e2e` = the same
 metric with the inputs copied from pinned host memory and the combined
 output copied back inside every step.  `--impl reference` times the CPU
 oracle (plain scalar C) on a bounded sample of the same workload instead.
@@ -59,6 +61,12 @@ def parse():
                     help="FP8 workloads: dispatch a pre-quantised payload (codes + scales)")
     ap.add_argument("--combine-dtype", choices=["bf16", "fp32", "fp8_e4m3"], default="bf16",
                     help="element type of the expert rows combine reads")
+    ap.add_argument("--split", action="store_true",
+                    help="split phases on two streams: dispatch_send / combine_recv on "
+                         "one, dispatch_recv / combine_send on the other")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch every step from the host instead of replaying a CUDA "
+                         "graph of it (per-kernel times always come from eager steps)")
     ap.add_argument("--combine-mode", choices=["gather", "scatter"], default="gather",
                     help="gather combine, or scatter combine through a staging area")
     ap.add_argument("--moe-group", type=int, default=0, metavar="GCAP",
@@ -293,6 +301,38 @@ def run_ours(args, rank, world, local_rank):
         if ev is not None:
             ev[3].record(stream)
 
+    stream2 = torch.cuda.Stream(device=dev)
+
+    def step_split(ev=None):
+        # sender side on `stream`, receiver / expert side on `stream2`
+        if ev is not None:
+            ev[0].record(stream)
+            ev[1].record(stream)
+        stream2.wait_stream(stream)
+        op.dispatch_send(x, w, xsc, idx, num_tokens=nt, stream=stream)
+        op.dispatch_recv(stream=stream2)
+        op.combine_send(stream=stream2)
+        if ev is not None:
+            ev[2].record(stream)
+        op.combine_recv(weights=op.out_w, out=out, out_weights=out_w, stream=stream)
+        stream.wait_stream(stream2)
+        if ev is not None:
+            ev[3].record(stream)
+
+    if args.split:
+        step = step_split   # noqa: F811  (split phases replace the one-stream step)
+
+    graph = None
+    if not args.eager:
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                step()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        torch.cuda.synchronize()
+
     sampler = ClockSampler(local_rank) if rank == 0 else None
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -309,7 +349,10 @@ def run_ours(args, rank, world, local_rank):
     with torch.cuda.stream(stream):
         start.record(stream)
         for i in range(args.steps):
-            step(evs[i])
+            if graph is not None:
+                graph.replay()
+            else:
+                step(evs[i])
         stop.record(stream)
     stop.synchronize()
     torch.cuda.synchronize()
@@ -317,6 +360,11 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     t_host1 = time.time()
     total_ms = start.elapsed_time(stop)
+    if graph is not None:   # per-kernel split: the same step run eagerly
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                step(evs[i])
+        torch.cuda.synchronize()
     lay = np.array([e[0].elapsed_time(e[1]) for e in evs])
     dis = np.array([e[1].elapsed_time(e[2]) for e in evs])
     com = np.array([e[2].elapsed_time(e[3]) for e in evs])
@@ -476,8 +524,12 @@ def run_ours(args, rank, world, local_rank):
             "l2": "every input and output is larger than L2 (x 470 MB, "
                   "dispatch out ~2.5 GB, combine in ~2.5 GB); no flush",
             "parallelism": f"replicas x{world}",
-            "step": "layout + dispatch_send (routing replay of that layout) + "
-                    "dispatch_recv + combine, one stream",
+            "step": ("dispatch_send (layout + copy) on stream A, dispatch_recv + "
+                     "combine_send on stream B, combine_recv on A" if args.split else
+                     "layout + dispatch_send (routing replay of that layout) + "
+                     "dispatch_recv + combine, one stream")
+                    + ("" if args.eager else
+                       "; timed as a CUDA-graph replay of the step (per-kernel times eager)"),
         },
         "gb_per_s": step_bytes / (ms_per_step / 1e3) / 1e9,
         "frac_of_nominal_8tbs": step_bytes / (ms_per_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
