@@ -16,7 +16,8 @@
 // slots; for each group of U column vectors (8 output elements each) a lane
 // issues the loads of ALL of the token's (<= MAXD) rows before it adds any,
 // so up to U * MAXD independent loads per lane are in flight, then it adds
-// them in rank order and writes 16 bytes of bf16.
+// them in rank order and writes 16 bytes of bf16.  FP8 rows go 16 codes per
+// lane-vector (one 16-byte load plus the block scale) and write 32 bytes.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -34,6 +35,12 @@ namespace {
 #endif
 #ifndef EP_COMBINE_UNROLL8
 #define EP_COMBINE_UNROLL8 2       // column vectors in flight per row, <= 8 rows
+#endif
+#ifndef EP_COMBINE_FP8_MIN_BLOCKS
+#define EP_COMBINE_FP8_MIN_BLOCKS 3   // FP8 rows (16-code vectors): <= 80 registers
+#endif
+#ifndef EP_COMBINE_FP8_UNROLL8
+#define EP_COMBINE_FP8_UNROLL8 1      // 16-code vectors in flight per row, <= 8 rows
 #endif
 
 constexpr int kCombineWarps = EP_COMBINE_WARPS;
@@ -71,25 +78,16 @@ __device__ __forceinline__ uint4 ld_coherent16(const void *p) {
                  : "memory");
     return v;
 }
-__device__ __forceinline__ uint2 ld_stream8(const void *p) {
-    uint2 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
-                 : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
-__device__ __forceinline__ uint2 ld_coherent8(const void *p) {
-    uint2 v;
-    asm volatile("ld.global.cs.v2.u32 {%0,%1}, [%2];"
-                 : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
-    return v;
-}
-
+// acc += the 8 bf16 values of v (exact widening, then two-wide fp32 adds).
 __device__ __forceinline__ void add_bf16x8(float acc[8], const uint4 &v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        acc[2 * i] = acc[2 * i] + __uint_as_float(w[i] << 16);
-        acc[2 * i + 1] = acc[2 * i + 1] + __uint_as_float(w[i] & 0xffff0000u);
+        const float2 r = add2_rn(make_float2(acc[2 * i], acc[2 * i + 1]),
+                                 make_float2(__uint_as_float(w[i] << 16),
+                                             __uint_as_float(w[i] & 0xffff0000u)));
+        acc[2 * i] = r.x;
+        acc[2 * i + 1] = r.y;
     }
 }
 
@@ -106,17 +104,18 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
     return __half22float2(__half2(h));
 }
 
-// acc += fl32(value(q) * scale) for 8 codes (no fused multiply-add).
-__device__ __forceinline__ void add_fp8x8(float acc[8], const uint2 &q, float scale) {
-    const uint32_t w[2] = {q.x, q.y};
+// acc += fl32(value(q) * scale) for 16 codes (a rounded multiply, then a
+// rounded add); acc[i] holds elements 2i, 2i+1.
+__device__ __forceinline__ void add_fp8x16(float2 acc[8], const uint4 &q, float scale) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
         const float2 lo = e4m3x2_to_float2(w[i] & 0xffffu);
         const float2 hi = e4m3x2_to_float2(w[i] >> 16);
-        acc[4 * i + 0] = __fadd_rn(acc[4 * i + 0], __fmul_rn(lo.x, scale));
-        acc[4 * i + 1] = __fadd_rn(acc[4 * i + 1], __fmul_rn(lo.y, scale));
-        acc[4 * i + 2] = __fadd_rn(acc[4 * i + 2], __fmul_rn(hi.x, scale));
-        acc[4 * i + 3] = __fadd_rn(acc[4 * i + 3], __fmul_rn(hi.y, scale));
+        acc[2 * i].x = __fadd_rn(acc[2 * i].x, __fmul_rn(lo.x, scale));
+        acc[2 * i].y = __fadd_rn(acc[2 * i].y, __fmul_rn(lo.y, scale));
+        acc[2 * i + 1].x = __fadd_rn(acc[2 * i + 1].x, __fmul_rn(hi.x, scale));
+        acc[2 * i + 1].y = __fadd_rn(acc[2 * i + 1].y, __fmul_rn(hi.y, scale));
     }
 }
 
@@ -145,27 +144,21 @@ __device__ void fused_receive_wait(const CombineParams &p) {
     __syncthreads();
 }
 
-// One row's share of a column vector: bf16 = one 16-byte load, fp32 = two,
-// FP8 = 8 code bytes plus the block scale (in a.z).
+// One row's share of a column vector: bf16 = one 16-byte load, fp32 = two.
 struct RowVec {
     uint4 a;
     uint4 b;
 };
 
 template <int YK, bool COHERENT>
-__device__ __forceinline__ RowVec load_vec(const char *row, const char *srow, int v) {
+__device__ __forceinline__ RowVec load_vec(const char *row, int v) {
     RowVec r;
     if constexpr (YK == kYBf16) {
         r.a = COHERENT ? ld_coherent16(row + (int64_t)v * 16) : ld_stream16(row + (int64_t)v * 16);
-    } else if constexpr (YK == kYF32) {
+    } else {
         r.a = COHERENT ? ld_coherent16(row + (int64_t)v * 32) : ld_stream16(row + (int64_t)v * 32);
         r.b = COHERENT ? ld_coherent16(row + (int64_t)v * 32 + 16)
                        : ld_stream16(row + (int64_t)v * 32 + 16);
-    } else {
-        const uint2 q = COHERENT ? ld_coherent8(row + (int64_t)v * 8) : ld_stream8(row + (int64_t)v * 8);
-        r.a.x = q.x;
-        r.a.y = q.y;
-        r.a.z = __float_as_uint(reinterpret_cast<const float *>(srow)[v >> 4]);
     }
     return r;
 }
@@ -174,16 +167,15 @@ template <int YK>
 __device__ __forceinline__ void add_vec(float acc[8], const RowVec &r) {
     if constexpr (YK == kYBf16) {
         add_bf16x8(acc, r.a);
-    } else if constexpr (YK == kYF32) {
+    } else {
         add_f32x4(acc, r.a);
         add_f32x4(acc + 4, r.b);
-    } else {
-        add_fp8x8(acc, make_uint2(r.a.x, r.a.y), __uint_as_float(r.a.z));
     }
 }
 
 template <int MAXD, int U, bool COHERENT, int YK, bool STAGED>
-__global__ void __launch_bounds__(kCombineThreads, EP_COMBINE_MIN_BLOCKS)
+__global__ void __launch_bounds__(kCombineThreads,
+                                  YK == kYFp8 ? EP_COMBINE_FP8_MIN_BLOCKS : EP_COMBINE_MIN_BLOCKS)
 combine_kernel(const CombineParams p) {
     // bytes of one column vector of an expert row: bf16 16, fp32 32, FP8 8
     constexpr int VB = YK == kYF32 ? 32 : (YK == kYFp8 ? 8 : 16);
@@ -236,6 +228,50 @@ combine_kernel(const CombineParams p) {
     }
 
     uint4 *out_row = reinterpret_cast<uint4 *>(p.out) + tok * p.nvec;
+    if constexpr (YK == kYFp8) {
+        // 16 codes (one 16-byte load) and their block's scale per lane-vector
+        const int nv = p.nvec >> 1;
+        for (int v0 = lane; v0 < nv; v0 += 32 * U) {
+            uint4 q[U][MAXD];
+            float sc[U][MAXD];
+#pragma unroll
+            for (int j = 0; j < MAXD; ++j) {
+                if (j < nd) {
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int v = v0 + 32 * u;
+                        if (v < nv) {
+                            q[u][j] = COHERENT ? ld_coherent16(rows[j] + (int64_t)v * 16)
+                                               : ld_stream16(rows[j] + (int64_t)v * 16);
+                            sc[u][j] = reinterpret_cast<const float *>(srows[j])[v >> 3];
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + 32 * u;
+                if (v >= nv) continue;
+                float2 acc[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = make_float2(0.0f, 0.0f);
+#pragma unroll
+                for (int j = 0; j < MAXD; ++j)
+                    if (j < nd) add_fp8x16(acc, q[u][j], sc[u][j]);
+                uint4 o0, o1;
+                o0.x = pack_bf16x2(acc[0].x, acc[0].y);
+                o0.y = pack_bf16x2(acc[1].x, acc[1].y);
+                o0.z = pack_bf16x2(acc[2].x, acc[2].y);
+                o0.w = pack_bf16x2(acc[3].x, acc[3].y);
+                o1.x = pack_bf16x2(acc[4].x, acc[4].y);
+                o1.y = pack_bf16x2(acc[5].x, acc[5].y);
+                o1.z = pack_bf16x2(acc[6].x, acc[6].y);
+                o1.w = pack_bf16x2(acc[7].x, acc[7].y);
+                st_stream16(out_row + 2 * v, o0);
+                st_stream16(out_row + 2 * v + 1, o1);
+            }
+        }
+    } else
     for (int v0 = lane; v0 < p.nvec; v0 += 32 * U) {
         RowVec val[U][MAXD];
 #pragma unroll
@@ -244,7 +280,7 @@ combine_kernel(const CombineParams p) {
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int v = v0 + 32 * u;
-                    if (v < p.nvec) val[u][j] = load_vec<YK, COHERENT>(rows[j], srows[j], v);
+                    if (v < p.nvec) val[u][j] = load_vec<YK, COHERENT>(rows[j], v);
                 }
             }
         }
@@ -466,7 +502,7 @@ template <int MAXD, int U>
 cudaError_t launch_combine_m(const Config &c, const CombineParams &p,
                              cudaStream_t st) {
     if (c.y_f32) return launch_combine_y<MAXD, (U > 1 ? U / 2 : 1), kYF32>(c, p, st);
-    if (c.y_fp8) return launch_combine_y<MAXD, U, kYFp8>(c, p, st);
+    if (c.y_fp8) return launch_combine_y<MAXD, (MAXD == 8 ? EP_COMBINE_FP8_UNROLL8 : U), kYFp8>(c, p, st);
     return launch_combine_y<MAXD, U, kYBf16>(c, p, st);
 }
 

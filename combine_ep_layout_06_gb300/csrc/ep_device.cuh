@@ -62,6 +62,22 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p,
     return old;
 }
 
+// Two-wide fp32 add: each half is the IEEE round-to-nearest scalar add
+// (subnormals kept), one instruction for the pair on this SM generation.
+// Only for sums of values that no multiply produced: measured on sm_103a
+// with CUDA 13.0, a two-wide round-to-nearest multiply feeding a two-wide
+// add could come out fused (one rounding), even with contraction disabled,
+// so products that must be rounded on their own stay scalar.
+__device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -18,8 +18,9 @@
 //          warp scan of the lanes' counts); the warps then read each payload
 //          row ONCE and store it (16-byte vectors) to each of its entry slots;
 //  ungroup one warp per received row: the loads of all its entries' rows for
-//          a column vector are in flight together, then the weighted fp32 sum
-//          in slot order (explicit __fmul_rn / __fadd_rn: no contraction).
+//          several column vectors are in flight together (more vectors when
+//          the row has fewer entries), then the weighted fp32 sum in slot
+//          order (a rounded multiply, then a rounded add: no contraction).
 #include <cuda_bf16.h>
 
 #include "ep_device.cuh"
@@ -217,6 +218,73 @@ __global__ void __launch_bounds__(kGroupWarps * 32) moe_group_kernel(const MoePa
     }
 }
 
+// Weighted fp32 sum of NE grouped rows (NE > 0 known: a fixed number of
+// entries, U column vectors per lane per pass) or of up to NE rows (the
+// general case, `ne` at run time).  Entries are taken in ascending top-k
+// slot j; the sum starts from +0 and each term is fl(w_j * y) (no FMA).
+template <int NE, int U, bool EXACT>
+__device__ __forceinline__ void ungroup_row(uint32_t em, int q, float w, const char *ybase,
+                                            uint4 *out, int nvec, int lane) {
+    const char *rows[NE];
+    float ws[NE];
+    int ne = 0;
+#pragma unroll
+    for (int i = 0; i < NE; ++i) {
+        rows[i] = nullptr;
+        ws[i] = 0.f;
+        if (em) {
+            const int j = __ffs(em) - 1;
+            em &= em - 1u;
+            const int qq = __shfl_sync(0xffffffffu, q, j);
+            ws[i] = __shfl_sync(0xffffffffu, w, j);
+            rows[i] = ybase + (int64_t)qq * nvec * 16;
+            ne = i + 1;
+        }
+    }
+    if (EXACT) ne = NE;
+    for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+        uint4 val[U][NE];
+#pragma unroll
+        for (int i = 0; i < NE; ++i)
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (i < ne && v0 + 32 * u < nvec)
+                    val[u][i] = ld_stream16(rows[i] + (int64_t)(v0 + 32 * u) * 16);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + 32 * u;
+            if (v >= nvec) continue;
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll
+            for (int i = 0; i < NE; ++i) {
+                if (i < ne) {
+                    const uint32_t wd[4] = {val[u][i].x, val[u][i].y, val[u][i].z, val[u][i].w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        acc[2 * h] = __fadd_rn(acc[2 * h],
+                                               __fmul_rn(ws[i], __uint_as_float(wd[h] << 16)));
+                        acc[2 * h + 1] = __fadd_rn(
+                            acc[2 * h + 1], __fmul_rn(ws[i], __uint_as_float(wd[h] & 0xffff0000u)));
+                    }
+                }
+            }
+            uint32_t pk[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+                pk[h] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * h])) |
+                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * h + 1])) << 16);
+            st_stream16(out + v, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+        }
+    }
+}
+
+// One warp per received row.  A row usually holds few entries (k over the
+// number of distinct destination ranks: ~1.5 for top-8 of 256 experts on 8
+// ranks), so the common counts get their own unrolled bodies with more
+// column vectors per lane: about 16 loads of 16 bytes in flight per lane
+// whatever the count.
 template <int MAXE, int U>
 __global__ void __launch_bounds__(kMoeWarps * 32) moe_ungroup_kernel(const MoeParams p,
                                                                      const char *yg,
@@ -236,62 +304,14 @@ __global__ void __launch_bounds__(kMoeWarps * 32) moe_ungroup_kernel(const MoePa
     }
     const uint32_t em = __ballot_sync(0xffffffffu, q >= 0 && q < p.gcap);
     const int nvec = p.H / 8;
-    const char *rows[MAXE];
-    float ws[MAXE];
-    int ne = 0;
-    {
-        uint32_t mm = em;
-#pragma unroll
-        for (int i = 0; i < MAXE; ++i) {
-            rows[i] = nullptr;
-            ws[i] = 0.f;
-            if (mm) {
-                const int j = __ffs(mm) - 1;
-                mm &= mm - 1u;
-                const int qq = __shfl_sync(0xffffffffu, q, j);
-                ws[i] = __shfl_sync(0xffffffffu, w, j);
-                rows[i] = yg + (int64_t)r * yg_stride + (int64_t)qq * nvec * 16;
-                ne = i + 1;
-            }
-        }
-    }
+    const char *ybase = yg + (int64_t)r * yg_stride;
     uint4 *out = reinterpret_cast<uint4 *>(const_cast<char *>(seg) + p.off_comb) + (int64_t)row * nvec;
-    // U column vectors per lane per pass: up to U * MAXE loads in flight
-    for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
-        uint4 val[U][MAXE];
-#pragma unroll
-        for (int i = 0; i < MAXE; ++i)
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (i < ne && v0 + 32 * u < nvec)
-                    val[u][i] = ld_stream16(rows[i] + (int64_t)(v0 + 32 * u) * 16);
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int v = v0 + 32 * u;
-            if (v >= nvec) continue;
-            float acc[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-#pragma unroll
-            for (int i = 0; i < MAXE; ++i) {
-                if (i < ne) {
-                    const uint32_t wd[4] = {val[u][i].x, val[u][i].y, val[u][i].z, val[u][i].w};
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        acc[2 * h] = __fadd_rn(acc[2 * h],
-                                               __fmul_rn(ws[i], __uint_as_float(wd[h] << 16)));
-                        acc[2 * h + 1] = __fadd_rn(
-                            acc[2 * h + 1], __fmul_rn(ws[i], __uint_as_float(wd[h] & 0xffff0000u)));
-                    }
-                }
-            }
-            uint32_t pk[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h)
-                pk[h] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * h])) |
-                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * h + 1])) << 16);
-            st_stream16(out + v, make_uint4(pk[0], pk[1], pk[2], pk[3]));
-        }
+    switch (__popc(em)) {
+    case 1: ungroup_row<1, 16, true>(em, q, w, ybase, out, nvec, lane); break;
+    case 2: ungroup_row<2, 8, true>(em, q, w, ybase, out, nvec, lane); break;
+    case 3: ungroup_row<3, 5, true>(em, q, w, ybase, out, nvec, lane); break;
+    case 4: ungroup_row<4, 4, true>(em, q, w, ybase, out, nvec, lane); break;
+    default: ungroup_row<MAXE, U, false>(em, q, w, ybase, out, nvec, lane); break;
     }
 }
 
