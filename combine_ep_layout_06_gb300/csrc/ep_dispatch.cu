@@ -49,6 +49,12 @@ namespace {
 #ifndef EP_DISPATCH_TPC
 #define EP_DISPATCH_TPC 2              // tokens per CTA, bulk path (divides 32)
 #endif
+#ifndef EP_DISPATCH_FP8_PREFETCH
+#define EP_DISPATCH_FP8_PREFETCH 1     // FP8: load the next element pair while quantising
+#endif
+#ifndef EP_FP8_RECIP_QUOT
+#define EP_FP8_RECIP_QUOT 1            // FP8: quotient by reciprocal + one FMA correction
+#endif
 #ifndef EP_DISPATCH_REG_TPC
 #define EP_DISPATCH_REG_TPC 4          // tokens per CTA, register / FP8 path
 #endif
@@ -191,6 +197,33 @@ __device__ __forceinline__ uint32_t quant4(const float *f, float scale) {
     return packed;
 }
 
+// fl32(x / scale) from r = RN(1 / scale) and one FMA correction of the
+// product (Markstein's division step: P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990).  For scale >= 2^-90 the residual x - q0*scale is exact
+// for every quotient large enough to give a nonzero code, and the E4M3 code
+// of the result equals that of the IEEE quotient for every bf16 x (checked
+// exhaustively over all bf16 x and block maxima); smaller scales divide.  The
+// sign of x is put back so that a quotient that is zero keeps the sign of x.
+__device__ __forceinline__ float quot_recip(float x, float scale, float r) {
+    const float q0 = __fmul_rn(x, r);
+    const float res = __fmaf_rn(-q0, scale, x);
+    return copysignf(__fmaf_rn(res, r, q0), x);
+}
+
+__device__ __forceinline__ uint32_t quant4_recip(const float *f, float scale, float r) {
+    uint32_t packed = 0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float a = quot_recip(f[2 * i], scale, r);
+        const float b = quot_recip(f[2 * i + 1], scale, r);
+        const __nv_fp8x2_storage_t q =
+            __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+        packed |= (uint32_t)q << (16 * i);
+    }
+    return packed;
+}
+
 // ------------------------------------------------------------ register path
 
 template <bool FP8, int U, int TPC>
@@ -249,6 +282,14 @@ dispatch_kernel(const DispatchParams p) {
             // lanes are either wholly in range or wholly out of it, and the
             // trip count is warp-uniform (the amax shuffles need all lanes).
             const int npair = p.nvec >> 1;
+#if EP_DISPATCH_FP8_PREFETCH
+            static_assert(U == 1, "prefetch of the next pair is for one pair per lane");
+            uint4 n0 = make_uint4(0u, 0u, 0u, 0u), n1 = n0;
+            if (lane < npair) {
+                n0 = ld_stream16(src + 2 * lane);
+                n1 = ld_stream16(src + 2 * lane + 1);
+            }
+#endif
             for (int base = 0; base < npair; base += 32 * U) {
                 uint4 q[U];
 #pragma unroll
@@ -256,10 +297,21 @@ dispatch_kernel(const DispatchParams p) {
                     const int pv = base + lane + 32 * u;
                     const bool active = pv < npair;
                     uint4 r0 = make_uint4(0u, 0u, 0u, 0u), r1 = r0;
+#if EP_DISPATCH_FP8_PREFETCH
+                    if (active) {
+                        r0 = n0;
+                        r1 = n1;
+                    }
+                    if (pv + 32 < npair) {
+                        n0 = ld_stream16(src + 2 * (pv + 32));
+                        n1 = ld_stream16(src + 2 * (pv + 32) + 1);
+                    }
+#else
                     if (active) {
                         r0 = ld_stream16(src + 2 * pv);
                         r1 = ld_stream16(src + 2 * pv + 1);
                     }
+#endif
                     float f[16];
                     unpack_bf16x8(r0, f);
                     unpack_bf16x8(r1, f + 8);
@@ -273,10 +325,21 @@ dispatch_kernel(const DispatchParams p) {
                     q[u] = make_uint4(0u, 0u, 0u, 0u);
                     if (a != 0.f) {
                         scale = a / 448.0f;
-                        q[u].x = quant4(f, scale);
-                        q[u].y = quant4(f + 4, scale);
-                        q[u].z = quant4(f + 8, scale);
-                        q[u].w = quant4(f + 12, scale);
+#if EP_FP8_RECIP_QUOT
+                        if (scale >= 0x1p-90f) {   // the same for the block's 8 lanes
+                            const float r = __frcp_rn(scale);
+                            q[u].x = quant4_recip(f, scale, r);
+                            q[u].y = quant4_recip(f + 4, scale, r);
+                            q[u].z = quant4_recip(f + 8, scale, r);
+                            q[u].w = quant4_recip(f + 12, scale, r);
+                        } else
+#endif
+                        {
+                            q[u].x = quant4(f, scale);
+                            q[u].y = quant4(f + 4, scale);
+                            q[u].z = quant4(f + 8, scale);
+                            q[u].w = quant4(f + 12, scale);
+                        }
                     }
                     if (active && (lane & 7) == 0) sm.scales[warp][pv >> 3] = scale;
                 }

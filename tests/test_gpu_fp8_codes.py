@@ -47,3 +47,56 @@ def test_fused_fp8_codes_match_the_oracle_everywhere():
         q, sc = oracle.quant_rows(inp.x_bits[s_, t_])
         assert np.array_equal(op.out[r, :n].cpu().numpy(), q), r
         assert np.array_equal(op.out_scales[r, :n].cpu().numpy().view(np.uint32), sc.view(np.uint32))
+
+
+def _every_value_under(maxima):
+    """Blocks of 128 bf16 values: block max A first, then every bf16
+    magnitude m <= A with both signs (zero-padded), for each A in maxima."""
+    blocks = []
+    for a in maxima:
+        mags = np.arange(0, a + 1, dtype=np.uint16)
+        vals = np.concatenate([mags, mags | np.uint16(0x8000)])
+        nblk = -(-vals.size // 127)
+        body = np.zeros(nblk * 127, np.uint16)
+        body[:vals.size] = vals
+        blk = np.empty((nblk, 128), np.uint16)
+        blk[:, 0] = a
+        blk[:, 1:] = body.reshape(nblk, 127)
+        blocks.append(blk)
+    return np.concatenate(blocks)
+
+
+def test_fused_fp8_codes_every_bf16_value_under_many_block_maxima():
+    """The quotient x / scale for every bf16 x (|x| <= block max A) under
+    510 maxima spanning every bf16 exponent (mantissa all-zero and all-one),
+    plus every maximum whose scale A/448 lies near 2^-90, where the kernel
+    switches between its reciprocal-and-correction quotient and a plain
+    IEEE division."""
+    maxima = [(e << 7) | m for e in range(255) for m in (0x00, 0x7F) if (e << 7) | m]
+    maxima += [(e << 7) | m for e in range(44, 48) for m in range(128)]
+    maxima = sorted(set(maxima))
+    blocks = _every_value_under(maxima)
+    H = 7168
+    per_row = H // 128
+    rows = -(-blocks.shape[0] // per_row)
+    W = 2
+    T = -(-rows // W)
+    pad = np.zeros((W * T * per_row - blocks.shape[0], 128), np.uint16)
+    x_bits = np.concatenate([blocks, pad]).reshape(W, T, H)
+    wl = gen.Workload("every_x", W, 2, 1, T, H, fp8=True)
+    inp = gen.make_inputs(wl)
+    inp.x_bits[...] = x_bits
+    op = make_op(wl)
+    x, w, idx = to_device(inp)
+    op.dispatch(x, w, None, idx)
+    torch.cuda.synchronize()
+    rc = op.recv_count.cpu().numpy()
+    assert int(rc.sum()) == W * T
+    for r in range(W):
+        n = int(rc[r])
+        src = op.src_pos[r, :n].cpu().numpy()
+        s_, t_ = np.divmod(src, wl.max_tokens_per_rank)
+        q, sc = oracle.quant_rows(inp.x_bits[s_, t_])
+        assert np.array_equal(op.out[r, :n].cpu().numpy(), q), r
+        assert np.array_equal(op.out_scales[r, :n].cpu().numpy().view(np.uint32), sc.view(np.uint32))
+    assert op.get_error() == (0, 0)
