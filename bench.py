@@ -458,10 +458,38 @@ def run_ours(args, rank, world, local_rank):
         d2h = hout[0].numel() * 2
         # the copied-back output equals the device result of the same inputs
         e2e_ok = bool(torch.equal(hout[(args.e2e_steps - 1) % 2].to(dev), out))
+        # The bound of a pipelined step: the same H2D and D2H bytes copied at
+        # once on the two copy streams with nothing else running.
+        lk = []
+        for _ in range(4):
+            torch.cuda.synchronize()
+            l0 = torch.cuda.Event(enable_timing=True)
+            l1 = torch.cuda.Event(enable_timing=True)
+            l0.record(s_in)
+            s_out.wait_event(l0)
+            with torch.cuda.stream(s_in):
+                dx[0].copy_(hx, non_blocking=True)
+                if dsc[0] is not None:
+                    dsc[0].copy_(hsc, non_blocking=True)
+                dw[0].copy_(hw, non_blocking=True)
+                di[0].copy_(hi, non_blocking=True)
+            with torch.cuda.stream(s_out):
+                hout[0].copy_(dout[0], non_blocking=True)
+            s_in.wait_stream(s_out)
+            l1.record(s_in)
+            l1.synchronize()
+            lk.append(l0.elapsed_time(l1))
+        link_ms = max_over_ranks(float(min(lk[1:])), world, dev)
         e2e = {"value": job_throughput(N, world, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e_ms, "pipelined": "H2D / compute / D2H on three streams",
-               "output_check": "pass" if e2e_ok else "FAIL"}
+               "output_check": "pass" if e2e_ok else "FAIL",
+               "host_link": {"copy_ms": link_ms,
+                             "h2d_gb_per_s": h2d / (link_ms / 1e3) / 1e9,
+                             "d2h_gb_per_s": d2h / (link_ms / 1e3) / 1e9,
+                             "frac": link_ms / e_ms,
+                             "what": "the step's H2D and D2H bytes copied concurrently, "
+                                     "alone: the bound of the pipelined step"}}
 
     moe = None
     if args.moe_group:
