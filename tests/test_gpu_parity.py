@@ -219,6 +219,76 @@ def test_graph_capture_replay_equals_eager():
     assert np.array_equal(op.recv_count.cpu().numpy(), eager["recv_count"])
 
 
+def test_routing_replay_after_one_call_dispatch():
+    """The one-call dispatch computes its layout inside the copy kernel and
+    leaves it for routing replay."""
+    wl = gen.WORKLOADS["dsv3"].scaled(96, hidden=512)
+    inp = gen.make_inputs(wl, num_tokens=gen.ragged_num_tokens(wl))
+    op = make_op(wl)
+    x, w, idx = to_device(inp)
+    nt = [int(n) for n in inp.num_tokens]
+    op.dispatch(x, w, None, idx, num_tokens=nt)
+    x2 = torch.randn_like(x, dtype=torch.float32).to(torch.bfloat16)
+    op.dispatch_send_replay(x2, w, idx, num_tokens=nt)
+    op.dispatch_recv()
+    torch.cuda.synchronize()
+    inp2 = gen.Inputs(wl, bits(x2).reshape(inp.x_bits.shape), inp.weights,
+                      inp.indices, inp.num_tokens)
+    ref = oracle.run_all(inp2, cap=op.cap)
+    assert np.array_equal(op.pos.cpu().numpy(), ref["pos"])
+    assert np.array_equal(op.send_counts.cpu().numpy(), ref["C"])
+    out = bits(op.out)
+    for r in range(wl.world_size):
+        n = ref["recv_count"][r]
+        assert np.array_equal(out[r, :n], ref["out"][r, :n])
+
+
+@pytest.mark.parametrize("name,fp8", [("ll_decode", False), ("dsv3", False), ("dsv3", True)])
+def test_captured_graph_replayed_on_new_routing(name, fp8):
+    """A captured one-call dispatch + combine replayed after the inputs were
+    overwritten in place (new tokens and routing, same shapes) gives the new
+    inputs' results: nothing of an earlier replay's layout is taken for the
+    current one."""
+    wl = gen.WORKLOADS[name].scaled(128 if name == "ll_decode" else 200, hidden=1024)
+    wl = gen.dataclasses.replace(wl, fp8=fp8)
+    inps = [gen.make_inputs(wl, seed=sd) for sd in (0, 7, 0)]
+    op = make_op(wl)
+    x, w, idx = to_device(inps[0])
+    nt = [int(n) for n in inps[0].num_tokens]
+    out = torch.empty((wl.world_size, wl.max_tokens_per_rank, wl.hidden),
+                      dtype=torch.bfloat16, device="cuda")
+    out_w = torch.empty((wl.world_size, wl.max_tokens_per_rank, wl.topk), device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        op.dispatch(x, w, None, idx, num_tokens=nt, stream=s)   # warm-up
+        op.identity_expert(stream=s)
+        op.combine(weights=op.out_w, out=out, out_weights=out_w, stream=s)
+        s.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            op.dispatch(x, w, None, idx, num_tokens=nt, stream=s)
+            op.identity_expert(stream=s)
+            op.combine(weights=op.out_w, out=out, out_weights=out_w, stream=s)
+    for inp in inps:
+        x2, w2, idx2 = to_device(inp)
+        x.copy_(x2)
+        w.copy_(w2)
+        idx.copy_(idx2)
+        out.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        res = oracle.run_all(inp, cap=op.cap)
+        assert np.array_equal(op.recv_count.cpu().numpy(), res["recv_count"])
+        assert np.array_equal(op.pos.cpu().numpy(), res["pos"])
+        got = bits(out)
+        for s_ in range(wl.world_size):
+            n = int(inp.num_tokens[s_])
+            assert np.array_equal(got[s_, :n], res["combined"][s_, :n]), s_
+    assert op.get_error() == (0, 0)
+
+
 # --------------------------------------------------------------- full size
 
 def _sample_check_full(wl, seed=0, n_rows=48, n_tok=24):
