@@ -15,8 +15,9 @@
 //  scan    one warp per (rank, expert): exclusive prefix over the chunks; the
 //          last CTA turns expert totals into per-rank offsets;
 //  group   one CTA per chunk: warp 0 derives every entry's slot (per-expert
-//          warp scan of the lanes' counts); the warps then read each payload
-//          row ONCE and store it (16-byte vectors) to each of its entry slots;
+//          warp scan of the lanes' counts); then each payload row is read
+//          ONCE and stored to each of its entry slots -- by TMA bulk copies
+//          through a shared-memory ring, or (long rows) by 16-byte vectors;
 //  ungroup one warp per received row: the loads of all its entries' rows for
 //          several column vectors are in flight together (more vectors when
 //          the row has fewer entries), then the weighted fp32 sum in slot
@@ -27,6 +28,10 @@
 
 namespace ep {
 namespace {
+
+#ifndef EP_MOE_GROUP_BULK_STAGES
+#define EP_MOE_GROUP_BULK_STAGES 4    // grouping by TMA bulk copies (0: register path)
+#endif
 
 constexpr int kMoeWarps = 8;
 constexpr int kGroupWarps = 4;
@@ -40,6 +45,7 @@ struct MoeParams {
     int32_t *cnt, *base, *count, *offset;
     uint32_t *words;
     int W, E, Er, k, H, cap, gcap, nrc, nb, row_bytes;
+    int64_t timeout_ns;        // bound of every mbarrier wait
 };
 
 __device__ __forceinline__ int rank_rows(const MoeParams &p, int r) {
@@ -140,41 +146,72 @@ struct GroupSmem {
     int32_t slot[kChunk][EP_MAX_TOPK];
 };
 
+// Warp 0: every entry slot of the chunk's 32 rows (per-expert warp scans
+// of the lanes' counts) into smem, and the entry-slot rows (-1: no entry).
+__device__ __forceinline__ void group_slots(const MoeParams &p, int r, int c, int n_r, char *seg,
+                                            GroupSmem &sm) {
+    const int lane = threadIdx.x & 31;
+    const int row = c * kChunk + lane;
+    int lid[EP_MAX_TOPK];
+    int slot[EP_MAX_TOPK];
+    local_experts(p, r, row, row < n_r, lid);
+    for (int j = 0; j < p.k; ++j) slot[j] = -1;
+    const int32_t *brow = p.base + ((int64_t)r * p.nrc + c) * p.Er;
+    for (int e = 0; e < p.Er; ++e) {
+        int ce = 0;
+        for (int j = 0; j < p.k; ++j) ce += (lid[j] == e);
+        if (!__any_sync(0xffffffffu, ce > 0)) continue;
+        int incl = ce;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += x;
+        }
+        int next = p.offset[r * p.Er + e] + brow[e] + incl - ce;
+        for (int j = 0; j < p.k; ++j)
+            if (lid[j] == e) slot[j] = next++;
+    }
+    for (int j = 0; j < p.k; ++j) sm.slot[lane][j] = slot[j];
+    if (row < p.cap) {
+        int32_t *es = reinterpret_cast<int32_t *>(seg + p.off_eslot) + (int64_t)row * p.k;
+        for (int j = 0; j < p.k; ++j) es[j] = slot[j];
+    }
+}
+
+// Metadata of row i's entries (one warp): source code p*k + j, weight, and
+// the FP8 block scales.
+__device__ __forceinline__ void group_metadata(const MoeParams &p, int row, int i, char *seg,
+                                               const GroupSmem &sm) {
+    const int lane = threadIdx.x & 31;
+    if (lane < p.k) {
+        const int q = sm.slot[i][lane];
+        if (q >= 0 && q < p.gcap) {
+            reinterpret_cast<int32_t *>(seg + p.off_gsrc)[q] = row * p.k + lane;
+            reinterpret_cast<float *>(seg + p.off_gw)[q] =
+                reinterpret_cast<const float *>(seg + p.off_w)[(int64_t)row * p.k + lane];
+        }
+    }
+    if (p.nb) {
+        const float *ssrc = reinterpret_cast<const float *>(seg + p.off_scales) + (int64_t)row * p.nb;
+        for (int j = 0; j < p.k; ++j) {
+            const int q = sm.slot[i][j];
+            if (q < 0 || q >= p.gcap) continue;
+            float *sdst = reinterpret_cast<float *>(seg + p.off_xgs) + (int64_t)q * p.nb;
+            for (int b = lane; b < p.nb; b += 32) sdst[b] = ssrc[b];
+        }
+    }
+}
+
+// Register path: the warps read each payload row once (16-byte vectors,
+// 4 in flight per lane) and store it to every entry slot.
 __global__ void __launch_bounds__(kGroupWarps * 32) moe_group_kernel(const MoeParams p) {
     __shared__ GroupSmem sm;
-    const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int r = blockIdx.x / p.nrc, c = blockIdx.x - r * p.nrc;
     const int n_r = rank_rows(p, r);
     char *seg = p.seg0 + (int64_t)r * p.seg_stride;
-
-    if (warp == 0) {
-        const int row = c * kChunk + lane;
-        int lid[EP_MAX_TOPK];
-        int slot[EP_MAX_TOPK];
-        local_experts(p, r, row, row < n_r, lid);
-        for (int j = 0; j < p.k; ++j) slot[j] = -1;
-        const int32_t *brow = p.base + ((int64_t)r * p.nrc + c) * p.Er;
-        for (int e = 0; e < p.Er; ++e) {
-            int ce = 0;
-            for (int j = 0; j < p.k; ++j) ce += (lid[j] == e);
-            if (!__any_sync(0xffffffffu, ce > 0)) continue;
-            int incl = ce;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int x = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += x;
-            }
-            int next = p.offset[r * p.Er + e] + brow[e] + incl - ce;
-            for (int j = 0; j < p.k; ++j)
-                if (lid[j] == e) slot[j] = next++;
-        }
-        for (int j = 0; j < p.k; ++j) sm.slot[lane][j] = slot[j];
-        if (row < p.cap) {
-            int32_t *es = reinterpret_cast<int32_t *>(seg + p.off_eslot) + (int64_t)row * p.k;
-            for (int j = 0; j < p.k; ++j) es[j] = slot[j];
-        }
-    }
+    if (warp == 0) group_slots(p, r, c, n_r, seg, sm);
     __syncthreads();
 
     const int nvec = p.row_bytes / 16;
@@ -182,24 +219,7 @@ __global__ void __launch_bounds__(kGroupWarps * 32) moe_group_kernel(const MoePa
         const int row = c * kChunk + i;
         if (row >= n_r) break;
         const uint4 *src = reinterpret_cast<const uint4 *>(seg + p.off_out) + (int64_t)row * nvec;
-        // metadata of each entry
-        if (lane < p.k) {
-            const int q = sm.slot[i][lane];
-            if (q >= 0 && q < p.gcap) {
-                reinterpret_cast<int32_t *>(seg + p.off_gsrc)[q] = row * p.k + lane;
-                reinterpret_cast<float *>(seg + p.off_gw)[q] =
-                    reinterpret_cast<const float *>(seg + p.off_w)[(int64_t)row * p.k + lane];
-            }
-        }
-        if (p.nb) {
-            const float *ssrc = reinterpret_cast<const float *>(seg + p.off_scales) + (int64_t)row * p.nb;
-            for (int j = 0; j < p.k; ++j) {
-                const int q = sm.slot[i][j];
-                if (q < 0 || q >= p.gcap) continue;
-                float *sdst = reinterpret_cast<float *>(seg + p.off_xgs) + (int64_t)q * p.nb;
-                for (int b = lane; b < p.nb; b += 32) sdst[b] = ssrc[b];
-            }
-        }
+        group_metadata(p, row, i, seg, sm);
         // payload: read once, store to every entry slot
         for (int v0 = lane; v0 < nvec; v0 += 32 * 4) {
             uint4 buf[4];
@@ -215,6 +235,80 @@ __global__ void __launch_bounds__(kGroupWarps * 32) moe_group_kernel(const MoePa
                     if (v0 + 32 * u < nvec) st_stream16(dst + v0 + 32 * u, buf[u]);
             }
         }
+    }
+}
+
+// Bulk path: thread 0 runs a ring of STAGES row buffers in shared memory;
+// each received row comes in once by cp.async.bulk (completion on an
+// mbarrier, bounded waits), then one bulk store per entry slot writes it
+// out, and a stage is refilled once the stores that read it are done
+// reading.  Warps 1.. write the entries' metadata meanwhile.
+template <int STAGES>
+__global__ void __launch_bounds__(kGroupWarps * 32) moe_group_bulk_kernel(const MoeParams p) {
+    extern __shared__ __align__(128) unsigned char gstage[];
+    __shared__ GroupSmem sm;
+    __shared__ __align__(8) uint64_t bar[STAGES];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x / p.nrc, c = blockIdx.x - r * p.nrc;
+    const int n_r = rank_rows(p, r);
+    char *seg = p.seg0 + (int64_t)r * p.seg_stride;
+    const int rows = max(0, min(kChunk, n_r - c * kChunk));
+    if (warp == 0) {
+        group_slots(p, r, c, n_r, seg, sm);
+        if (lane == 0) {
+            for (int i = 0; i < STAGES; ++i) mbar_init(&bar[i], 1);
+            mbar_init_fence();
+        }
+    }
+    __syncthreads();
+    if (rows == 0) return;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint32_t bytes = (uint32_t)p.row_bytes;
+            const uint64_t pol = l2_evict_first_policy();
+            auto issue = [&](int i) {
+                const int st = i % STAGES;
+                mbar_expect_tx(&bar[st], bytes);
+                bulk_load(gstage + (size_t)st * bytes,
+                          seg + p.off_out + ((int64_t)c * kChunk + i) * bytes, bytes, &bar[st], pol);
+            };
+            const int pre = rows < STAGES ? rows : STAGES;
+            for (int i = 0; i < pre; ++i) issue(i);
+            int issued = pre;
+            bool ok = true;
+            for (int i = 0; i < rows; ++i) {
+                const int st = i % STAGES;
+                if (!mbar_wait(&bar[st], (uint32_t)(i / STAGES) & 1u, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                const unsigned char *src = gstage + (size_t)st * bytes;
+                for (int j = 0; j < p.k; ++j) {
+                    const int q = sm.slot[i][j];
+                    if (q >= 0 && q < p.gcap)
+                        bulk_store(seg + p.off_xg + (int64_t)q * bytes, src, bytes, pol);
+                }
+                bulk_commit();
+                // the stage of row i-1: its stores were committed one group ago
+                if (i >= 1 && issued < rows) {
+                    bulk_wait_read1();
+                    issue(issued);
+                    ++issued;
+                }
+            }
+            if (!ok) {
+                set_error(p.words, EP_DEVERR_TIMEOUT);
+                for (int i = 0; i < issued; ++i)   // no copy may outlive the CTA
+                    mbar_wait(&bar[i % STAGES], (uint32_t)(i / STAGES) & 1u, p.timeout_ns);
+            }
+            bulk_wait_all();
+        }
+        __syncwarp();
+    } else {
+        for (int i = warp - 1; i < rows; i += kGroupWarps - 1)
+            group_metadata(p, c * kChunk + i, i, seg, sm);
     }
 }
 
@@ -338,6 +432,7 @@ MoeParams make_params(const Config &c, const Workspace &ws) {
     p.W = c.W; p.E = c.E; p.Er = c.Er; p.k = c.k; p.H = c.H; p.cap = c.cap;
     p.gcap = c.gcap; p.nrc = c.nrc; p.nb = c.nb;
     p.row_bytes = c.fp8 ? c.H : c.H * 2;
+    p.timeout_ns = c.timeout_ns;
     return p;
 }
 
@@ -349,6 +444,25 @@ cudaError_t launch_moe_group(const Config &c, const Workspace &ws, cudaStream_t 
     moe_count_kernel<<<(chunks + kMoeWarps - 1) / kMoeWarps, kMoeWarps * 32, 0, st>>>(p);
     const int seqs = c.W * c.Er;
     moe_scan_kernel<<<(seqs + kMoeWarps - 1) / kMoeWarps, kMoeWarps * 32, 0, st>>>(p);
+#if EP_MOE_GROUP_BULK_STAGES > 0
+    const size_t dyn = (size_t)EP_MOE_GROUP_BULK_STAGES * p.row_bytes;
+    if (dyn <= 160 * 1024) {
+        constexpr int kMaxDevices = 64;     // function attributes are per device
+        static size_t configured[kMaxDevices] = {};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+        if (dyn > configured[dev]) {
+            e = cudaFuncSetAttribute(moe_group_bulk_kernel<EP_MOE_GROUP_BULK_STAGES>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+            if (e != cudaSuccess) return e;
+            configured[dev] = dyn;
+        }
+        moe_group_bulk_kernel<EP_MOE_GROUP_BULK_STAGES><<<chunks, kGroupWarps * 32, dyn, st>>>(p);
+        return cudaGetLastError();
+    }
+#endif
     moe_group_kernel<<<chunks, kGroupWarps * 32, 0, st>>>(p);
     return cudaGetLastError();
 }
