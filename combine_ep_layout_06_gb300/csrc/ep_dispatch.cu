@@ -504,16 +504,20 @@ constexpr int kBulkStages =
 // min(W,k) destinations x the row, >= 64 KB), fewer bulk-copy CTAs per SM --
 // fewer concurrent row streams per SM -- measured faster than filling every
 // slot, so the dynamic shared memory is padded until at most
-// EP_DISPATCH_BULK_CTAS_PER_SM CTAs fit.  Small rows or few destinations
-// keep full residency (per-CTA set-up would dominate otherwise).
+// max(EP_DISPATCH_BULK_CTAS_PER_SM, kBulkStreamBytes / row) CTAs fit: two
+// CTAs per SM for 14 KB rows, four for 7 KB E4M3 code rows.  Small rows or
+// few destinations keep full residency (per-CTA set-up would dominate).
+constexpr size_t kBulkStreamBytes = 2 * 14336;
+
 template <int STAGES, int TPC>
 cudaError_t launch_dispatch_bulk(const Config &c, const DispatchParams &p,
                                  cudaStream_t st) {
     // Function attributes are per device: cache the opted-in size and the
-    // capped-residency share per device.
+    // shared-memory figures per device.
     constexpr int kMaxDevices = 64;
     static size_t configured[kMaxDevices] = {};
-    static long share[kMaxDevices] = {};
+    static long per_sm[kMaxDevices] = {};
+    static long fixed[kMaxDevices] = {};     // reserved + static shared memory per CTA
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -522,20 +526,22 @@ cudaError_t launch_dispatch_bulk(const Config &c, const DispatchParams &p,
     size_t dyn = (size_t)STAGES * row;
     const size_t per_cta = (size_t)TPC * (size_t)(c.W < c.k ? c.W : c.k) * row;
     if (EP_DISPATCH_BULK_CTAS_PER_SM > 0 && per_cta >= 64 * 1024) {
-        if (share[dev] == 0) {
-            int per_sm = 0, reserved = 0;
+        if (per_sm[dev] == 0) {
+            int sm_bytes = 0, reserved = 0;
             cudaFuncAttributes fa;
-            if ((e = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+            if ((e = cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
                                             dev)) != cudaSuccess ||
                 (e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock,
                                             dev)) != cudaSuccess ||
                 (e = cudaFuncGetAttributes(&fa, dispatch_bulk_kernel<STAGES, TPC>)) != cudaSuccess)
                 return e;
-            const long v = (long)per_sm / EP_DISPATCH_BULK_CTAS_PER_SM - reserved -
-                           (long)fa.sharedSizeBytes;
-            share[dev] = v > 0 ? (v & ~127L) : -1;
+            fixed[dev] = (long)reserved + (long)fa.sharedSizeBytes;
+            per_sm[dev] = sm_bytes;
         }
-        if (share[dev] > 0 && (size_t)share[dev] > dyn) dyn = (size_t)share[dev];
+        long ctas = (long)(kBulkStreamBytes / row);
+        if (ctas < EP_DISPATCH_BULK_CTAS_PER_SM) ctas = EP_DISPATCH_BULK_CTAS_PER_SM;
+        const long share = (per_sm[dev] / ctas - fixed[dev]) & ~127L;
+        if (share > 0 && (size_t)share > dyn) dyn = (size_t)share;
     }
     if (dyn > configured[dev]) {        // opt in to the dynamic size
         e = cudaFuncSetAttribute(dispatch_bulk_kernel<STAGES, TPC>,
