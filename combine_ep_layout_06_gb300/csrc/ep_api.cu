@@ -281,6 +281,7 @@ static ep_status_t dispatch_send_impl(ep_handle_t *h, const void *d_x,
     a.idx = d_idx;
     a.nt = nt;
     a.epoch = h->dispatch_epoch;
+    a.after_layout = run_layout;
     return gpu(h, launch_dispatch(h->cfg, h->ws, a, st), "dispatch");
 }
 

@@ -78,6 +78,16 @@ __device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
     return d;
 }
 
+// Programmatic dependent launch: the dependent grid may start once every CTA
+// of this one has signalled; griddepcontrol.wait blocks until the grid it
+// depends on has completed and its memory is visible (no-op otherwise).
+__device__ __forceinline__ void grid_dependents_may_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

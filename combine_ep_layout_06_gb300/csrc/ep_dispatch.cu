@@ -52,6 +52,9 @@ namespace {
 #ifndef EP_FP8_RECIP_QUOT
 #define EP_FP8_RECIP_QUOT 1            // FP8: quotient by reciprocal + one FMA correction
 #endif
+#ifndef EP_DISPATCH_PDL
+#define EP_DISPATCH_PDL 1              // launch the copy programmatically after the layout
+#endif
 #ifndef EP_DISPATCH_REG_TPC
 #define EP_DISPATCH_REG_TPC 4          // tokens per CTA, register / FP8 path
 #endif
@@ -236,6 +239,7 @@ dispatch_kernel(const DispatchParams p) {
     const int t0 = (g - s * p.nch) * kChunk;
     const int n_s = p.nt.n[s];
 
+    grid_dependency_wait();
     if (warp == 0) chunk_slots<TPC>(p, g, s, t0, n_s, i0, sm.pos, sm.mask);
     __syncthreads();
 
@@ -396,35 +400,36 @@ dispatch_bulk_kernel(const DispatchParams p) {
     const int t0 = (g - s * p.nch) * kChunk;
     const int n_s = p.nt.n[s];
 
-    if (warp == 0) {
-        chunk_slots<TPC>(p, g, s, t0, n_s, i0, sm.pos, sm.mask);
-        __syncwarp();
-        if (lane == 0) {
-            int n = 0;
-            for (int i = i0; i < i0 + TPC; ++i)
-                if (t0 + i < n_s && sm.mask[i]) sm.list[n++] = i;
-            s_n = n;
-            for (int i = 0; i < STAGES; ++i) mbar_init(&bar[i], 1);
-            mbar_init_fence();
-        }
+    // The CTA's rows are its tokens below n_s.  Their loads do not depend on
+    // the layout, so thread 0 issues them before waiting for it: launched
+    // programmatically after the layout kernel, they overlap its tail.
+    const uint32_t bytes = (uint32_t)p.row_bytes;
+    auto issue = [&](int j, uint64_t pol) {
+        const int st = j % STAGES;
+        const char *src = reinterpret_cast<const char *>(p.x) +
+                          ((int64_t)s * p.T + t0 + sm.list[j]) * bytes;
+        mbar_expect_tx(&bar[st], bytes);
+        bulk_load(stage_buf + (size_t)st * bytes, src, bytes, &bar[st], pol);
+    };
+    if (threadIdx.x == 0) {
+        int n = 0;
+        for (int i = i0; i < i0 + TPC; ++i)
+            if (t0 + i < n_s) sm.list[n++] = i;
+        s_n = n;
+        for (int i = 0; i < STAGES; ++i) mbar_init(&bar[i], 1);
+        mbar_init_fence();
+        const uint64_t pol = l2_evict_first_policy();
+        for (int j = 0; j < (n < STAGES ? n : STAGES); ++j) issue(j, pol);
     }
+    grid_dependency_wait();
+    if (warp == 0) chunk_slots<TPC>(p, g, s, t0, n_s, i0, sm.pos, sm.mask);
     __syncthreads();
     const int n = s_n;
 
     if (warp == 0) {
         if (lane == 0) {
-            const uint32_t bytes = (uint32_t)p.row_bytes;
             const uint64_t pol = l2_evict_first_policy();
-            auto issue = [&](int j) {
-                const int st = j % STAGES;
-                const char *src = reinterpret_cast<const char *>(p.x) +
-                                  ((int64_t)s * p.T + t0 + sm.list[j]) * bytes;
-                mbar_expect_tx(&bar[st], bytes);
-                bulk_load(stage_buf + (size_t)st * bytes, src, bytes, &bar[st], pol);
-            };
-            const int pre = n < STAGES ? n : STAGES;
-            for (int j = 0; j < pre; ++j) issue(j);
-            int issued = pre;
+            int issued = n < STAGES ? n : STAGES;
             bool ok = true;
             for (int j = 0; j < n; ++j) {
                 const int st = j % STAGES;
@@ -449,7 +454,7 @@ dispatch_bulk_kernel(const DispatchParams p) {
                 // reading frees it
                 if (j >= 1 && issued < n) {
                     bulk_wait_read1();
-                    issue(issued);
+                    issue(issued, pol);
                     ++issued;
                 }
             }
@@ -489,11 +494,29 @@ __global__ void dispatch_recv_kernel(uint32_t *dflags, uint32_t *words,
     if (tid < W) recv_count[tid] = totals[tid];
 }
 
+// Launch, programmatically dependent on the kernel before it when that is the
+// layout kernel: the copy kernel's CTAs start while the layout finishes and
+// wait for its results with griddepcontrol.wait.
+template <typename Kernel>
+cudaError_t launch_copy(Kernel kernel, int blocks, size_t dyn, bool after_layout,
+                        const DispatchParams &p, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kDispatchThreads);
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = after_layout ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 template <bool FP8, int U, int TPC>
-cudaError_t launch_dispatch_t(const Config &c, const DispatchParams &p,
+cudaError_t launch_dispatch_t(const Config &c, const DispatchParams &p, bool after_layout,
                               cudaStream_t st) {
-    dispatch_kernel<FP8, U, TPC><<<c.G * (kChunk / TPC), kDispatchThreads, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_copy(dispatch_kernel<FP8, U, TPC>, c.G * (kChunk / TPC), 0, after_layout, p, st);
 }
 
 // The ring never needs more stages than the CTA has tokens.
@@ -510,7 +533,7 @@ constexpr int kBulkStages =
 constexpr size_t kBulkStreamBytes = 2 * 14336;
 
 template <int STAGES, int TPC>
-cudaError_t launch_dispatch_bulk(const Config &c, const DispatchParams &p,
+cudaError_t launch_dispatch_bulk(const Config &c, const DispatchParams &p, bool after_layout,
                                  cudaStream_t st) {
     // Function attributes are per device: cache the opted-in size and the
     // shared-memory figures per device.
@@ -549,8 +572,8 @@ cudaError_t launch_dispatch_bulk(const Config &c, const DispatchParams &p,
         if (e != cudaSuccess) return e;
         configured[dev] = dyn;
     }
-    dispatch_bulk_kernel<STAGES, TPC><<<c.G * (kChunk / TPC), kDispatchThreads, dyn, st>>>(p);
-    return cudaGetLastError();
+    return launch_copy(dispatch_bulk_kernel<STAGES, TPC>, c.G * (kChunk / TPC), dyn, after_layout,
+                       p, st);
 }
 
 }  // namespace
@@ -582,16 +605,17 @@ cudaError_t launch_dispatch(const Config &c, const Workspace &ws,
     p.epoch = a.epoch;
     p.timeout_ns = c.timeout_ns;
     p.nt = a.nt;
+    const bool pdl = a.after_layout && EP_DISPATCH_PDL;
     if (c.fp8 && !a.scales_in)      // fused quantisation
-        return launch_dispatch_t<true, EP_DISPATCH_FP8_UNROLL, EP_DISPATCH_REG_TPC>(c, p, st);
+        return launch_dispatch_t<true, EP_DISPATCH_FP8_UNROLL, EP_DISPATCH_REG_TPC>(c, p, pdl, st);
     // rows copied unchanged: bf16, or pre-quantised codes (H <= 16384 bytes)
 #if EP_DISPATCH_BULK_STAGES > 0
     if ((size_t)kBulkStages * p.row_bytes <= 160 * 1024)
-        return launch_dispatch_bulk<kBulkStages, EP_DISPATCH_TPC>(c, p, st);
+        return launch_dispatch_bulk<kBulkStages, EP_DISPATCH_TPC>(c, p, pdl, st);
 #endif
     if (c.fp8)   // the register path copies bf16-sized vectors: not for codes
         return cudaErrorInvalidValue;
-    return launch_dispatch_t<false, EP_DISPATCH_UNROLL, EP_DISPATCH_REG_TPC>(c, p, st);
+    return launch_dispatch_t<false, EP_DISPATCH_UNROLL, EP_DISPATCH_REG_TPC>(c, p, pdl, st);
 }
 
 cudaError_t launch_dispatch_recv(const Config &c, const Workspace &ws,

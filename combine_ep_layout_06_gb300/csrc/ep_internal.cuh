@@ -90,6 +90,7 @@ struct DispatchArgs {
     const int32_t *idx;    // [W][T][k]
     TokenCounts nt;
     uint32_t epoch;        // flag value when early_notify
+    bool after_layout;     // launched right after the layout kernel on the same stream
 };
 cudaError_t launch_dispatch(const Config &c, const Workspace &ws,
                             const DispatchArgs &a, cudaStream_t st);

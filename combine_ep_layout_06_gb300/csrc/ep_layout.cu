@@ -50,6 +50,9 @@ layout_kernel(const LayoutParams p) {
     const int warp = threadIdx.x >> 5;
     const int q = blockIdx.x;
     const int g = q * kGroup + warp;
+    // the copy kernel launched after this one may start now: its CTAs load
+    // their rows and then wait for this grid's results
+    grid_dependents_may_launch();
 
     // ---- per chunk: masks and destination counts (warp ballot)
     int my_count = 0;
