@@ -36,6 +36,9 @@ namespace {
 #ifndef EP_COMBINE_UNROLL8
 #define EP_COMBINE_UNROLL8 2       // column vectors in flight per row, <= 8 rows
 #endif
+#ifndef EP_COMBINE_PDL
+#define EP_COMBINE_PDL 1              // launch programmatically after the previous kernel
+#endif
 #ifndef EP_COMBINE_FP8_MIN_BLOCKS
 #define EP_COMBINE_FP8_MIN_BLOCKS 3   // FP8 rows (16-code vectors): <= 80 registers
 #endif
@@ -179,6 +182,7 @@ __global__ void __launch_bounds__(kCombineThreads,
 combine_kernel(const CombineParams p) {
     // bytes of one column vector of an expert row: bf16 16, fp32 32, FP8 8
     constexpr int VB = YK == kYF32 ? 32 : (YK == kYFp8 ? 8 : 16);
+    grid_dependency_wait();   // launched programmatically: the rows are complete from here
     if (p.fused_wait) fused_receive_wait(p);
 
     const int lane = threadIdx.x & 31;
@@ -482,6 +486,15 @@ cudaError_t launch_combine_t(const Config &c, const CombineParams &p,
                              cudaStream_t st) {
     const int64_t tokens = (int64_t)c.W * c.T;
     const int blocks = (int)((tokens + kCombineWarps - 1) / kCombineWarps);
+#if EP_COMBINE_PDL
+    if constexpr (YK == kYBf16) {
+        if (p.stage)
+            return launch_after_previous(combine_kernel<MAXD, U, COH, YK, true>, blocks,
+                                         kCombineThreads, 0, st, p);
+    }
+    return launch_after_previous(combine_kernel<MAXD, U, COH, YK, false>, blocks, kCombineThreads,
+                                 0, st, p);
+#else
     if constexpr (YK == kYBf16) {
         if (p.stage) {
             combine_kernel<MAXD, U, COH, YK, true><<<blocks, kCombineThreads, 0, st>>>(p);
@@ -490,6 +503,7 @@ cudaError_t launch_combine_t(const Config &c, const CombineParams &p,
     }
     combine_kernel<MAXD, U, COH, YK, false><<<blocks, kCombineThreads, 0, st>>>(p);
     return cudaGetLastError();
+#endif
 }
 
 template <int MAXD, int U, int YK>

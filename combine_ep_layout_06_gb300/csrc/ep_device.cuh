@@ -199,4 +199,23 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Launch `kernel` programmatically dependent on the kernel before it on the
+// stream: its CTAs may be scheduled while that kernel finishes and must call
+// grid_dependency_wait() before reading anything it (or earlier work) wrote.
+template <typename... Params, typename... Args>
+cudaError_t launch_after_previous(void (*kernel)(Params...), unsigned blocks, unsigned threads,
+                                  size_t dyn, cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 }  // namespace ep
