@@ -549,12 +549,7 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "fp8" if wl.fp8 else "bf16",
         "data": "synthetic (seeded; shapes and routing of the workload, no dataset)",
         "config": {
-            "workload": f"{wl.name}: W={W} logical ranks on one GPU, E={wl.num_experts}, "
-                        f"k={k}, T={T} tokens/rank, H={H}, "
-                        f"{'fp8 e4m3' if wl.fp8 else 'bf16'} dispatch"
-                        f"{' of a pre-quantised payload' if args.fp8_input else ''}, "
-                        f"fp32-accumulate bf16 combine of {args.combine_dtype} expert rows "
-                        f"with weights, {wl.routing} routing",
+            "workload": workload_text(wl, args),
             "tokens_per_step": N,
             "routed_pairs": P,
             "l2": "every input and output is larger than L2 (x 470 MB, "
@@ -632,6 +627,16 @@ def cpu_baseline(wl, inp, repeats=1):
             "seconds": tsec}
 
 
+def workload_text(wl, args):
+    """The workload as both arms name it in `config`."""
+    return (f"{wl.name}: W={wl.world_size} logical ranks on one GPU, E={wl.num_experts}, "
+            f"k={wl.topk}, T={wl.max_tokens_per_rank} tokens/rank, H={wl.hidden}, "
+            f"{'fp8 e4m3' if wl.fp8 else 'bf16'} dispatch"
+            f"{' of a pre-quantised payload' if args.fp8_input else ''}, "
+            f"fp32-accumulate bf16 combine of {args.combine_dtype} expert rows "
+            f"with weights, {wl.routing} routing")
+
+
 def run_reference(args):
     """--impl reference: the CPU oracle, timed per step on a bounded sample."""
     import oracle
@@ -660,12 +665,14 @@ def run_reference(args):
     v = n / tsec
     return {
         "impl": "reference",
-        "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
+        "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": steps, "warmup": args.warmup, "ms_per_step": tsec * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8" if wl.fp8 else "bf16", "data": "synthetic",
-        "config": {"workload": f"{wl.name} recipe, oracle sample of {sample} "
-                               f"tokens/rank ({n} tokens) per step"},
+        "config": {"workload": workload_text(wl, args),
+                   "tokens_per_step": wl.world_size * wl.max_tokens_per_rank,
+                   "sample": f"each timed step runs the oracle on {sample} tokens/rank "
+                             f"({n} tokens) of this workload; value = tokens/s of that sample"},
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1,
                          "kind": "oracle",
                          "sample": f"{n} tokens of the {wl.name} recipe per step"},
