@@ -19,6 +19,16 @@ pytestmark = pytest.mark.gpu
 def test_fp8_combine_payload_parity(name, T, H, ragged):
     wl = gen.WORKLOADS[name].scaled(T, hidden=H)
     inp = gen.make_inputs(wl, num_tokens=gen.ragged_num_tokens(wl) if ragged else None)
+    _check_fp8_combine(wl, inp)
+
+
+def test_fp8_combine_payload_wide_topk():
+    """32 destination ranks per token: the 32-row FP8 gather."""
+    wl = gen.Workload("wide", 32, 64, 32, 40, 256)
+    _check_fp8_combine(wl, gen.make_inputs(wl, num_tokens=gen.ragged_num_tokens(wl)))
+
+
+def _check_fp8_combine(wl, inp):
     op = make_op(wl, combine_dtype="fp8_e4m3")
     x, w, idx = to_device(inp)
     op.dispatch(x, w, None, idx, num_tokens=[int(n) for n in inp.num_tokens])

@@ -76,6 +76,19 @@ def test_moe_grouping_parity(name, T, H, ragged):
     assert op.get_error() == (0, 0)
 
 
+@pytest.mark.parametrize("W,E,k", [(2, 32, 12), (2, 64, 32)])
+def test_moe_grouping_many_entries_per_row(W, E, k):
+    """Rows holding more than 8 entries: the un-grouping's 16- and 32-entry
+    bodies (and, with duplicates, up to k entries of one expert)."""
+    wl = gen.Workload("many", W, E, k, 60, 256)
+    inp = gen.make_inputs(wl)
+    if k > E // W:
+        rng = np.random.default_rng(3)
+        inp.indices[...] = rng.integers(0, E, size=inp.indices.shape)
+    op, _ = _group_and_check(wl, inp, random_y=True)
+    assert op.get_error() == (0, 0)
+
+
 def test_moe_grouping_duplicates_and_random_expert_outputs():
     wl = gen.Workload("dupg", 4, 16, 5, 70, 256)
     inp = gen.make_inputs(wl)

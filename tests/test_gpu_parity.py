@@ -120,6 +120,30 @@ def test_parity_duplicate_experts_and_wide_world():
     _compare(wl, inp, run_gpu(op, inp), op.cap)
 
 
+@pytest.mark.parametrize("W,E,k,fp8", [(16, 32, 12, False), (32, 64, 32, False),
+                                        (32, 64, 32, True)])
+def test_parity_wide_topk(W, E, k, fp8):
+    """More than 8 destination ranks per token: the combine's 16- and 32-row
+    gathers, one stream and split with the fused receive."""
+    wl = gen.Workload("wide", W, E, k, 40, 256, fp8=fp8)
+    inp = gen.make_inputs(wl, num_tokens=gen.ragged_num_tokens(wl))
+    op = make_op(wl)
+    _compare(wl, inp, run_gpu(op, inp), op.cap)
+    op2 = make_op(wl, early_notify=True, fused_recv=True)
+    _compare(wl, inp, run_gpu(op2, inp, split=True), op2.cap)
+    assert op.get_error() == (0, 0) and op2.get_error() == (0, 0)
+
+
+def test_parity_long_rows_take_the_register_copy():
+    """bf16 rows of 88 KB do not fit the bulk copy's shared-memory ring; the
+    register copy moves them."""
+    wl = gen.Workload("long", 2, 4, 2, 40, 45056)
+    inp = gen.make_inputs(wl, num_tokens=gen.ragged_num_tokens(wl))
+    op = make_op(wl)
+    _compare(wl, inp, run_gpu(op, inp), op.cap)
+    assert op.get_error() == (0, 0)
+
+
 def test_empty_batch():
     wl = gen.WORKLOADS["tiny"]
     inp = gen.make_inputs(wl, num_tokens=[0, 0])

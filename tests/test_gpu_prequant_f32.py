@@ -84,6 +84,17 @@ def test_fp32_combine_parity(name, ragged):
     T = {"dsv3": 150, "dsv3_fp8_zipf": 150, "mixtral": 200, "ll_decode": 128}[name]
     wl = gen.WORKLOADS[name].scaled(T, hidden=1024)
     inp = gen.make_inputs(wl, num_tokens=gen.ragged_num_tokens(wl) if ragged else None)
+    _check_fp32_combine(wl, inp)
+
+
+@pytest.mark.parametrize("W,E,k", [(16, 32, 12), (32, 64, 32)])
+def test_fp32_combine_wide_topk(W, E, k):
+    """More than 8 destination ranks per token: the 16- and 32-row fp32 gathers."""
+    wl = gen.Workload("wide", W, E, k, 40, 256)
+    _check_fp32_combine(wl, gen.make_inputs(wl, num_tokens=gen.ragged_num_tokens(wl)))
+
+
+def _check_fp32_combine(wl, inp):
     op = make_op(wl, combine_dtype="fp32")
     x, w, idx = to_device(inp)
     op.dispatch(x, w, None, idx, num_tokens=[int(n) for n in inp.num_tokens])
