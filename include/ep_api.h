@@ -204,7 +204,11 @@ ep_status_t ep_layout(ep_handle_t *h, const int32_t *d_idx,
  *    `scales` beside `input` and "can carry already-quantized FP8
  *    payloads"): d_x is [W][T][H] E4M3 codes and d_scales [W][T][H/128]
  *    fp32 block scales, both copied unchanged.
- * Inputs must stay unchanged until the receive phase has been enqueued. */
+ * Inputs must stay unchanged until the receive phase has been enqueued.
+ * The copy kernel is launched as a programmatic dependent of the layout
+ * kernel just before it (both enqueued by this call), so stream capture
+ * records a programmatic edge between them; anything enqueued earlier on
+ * the stream is complete before either starts. */
 ep_status_t ep_dispatch_send(ep_handle_t *h, const void *d_x, const float *d_w,
                              const float *d_scales, const int32_t *d_idx,
                              const int32_t *h_num_tokens, void *stream);
@@ -259,7 +263,10 @@ ep_status_t ep_combine_send(ep_handle_t *h, void *stream);
  * dispatch (checked: a token whose destination set differs sets the
  * COMBINE_MISMATCH bit; the dispatch's layout is used).  d_out: [W][T][H]
  * bf16; d_out_w: [W][T][k] fp32 (written iff d_w_in).  Rows t >= n_s are
- * not written.  BAD_STATE without a dispatch or without a combine send. */
+ * not written.  BAD_STATE without a dispatch or without a combine send.
+ * The gather kernel is launched as a programmatic dependent of the kernel
+ * before it on the stream and waits for that kernel's completion before
+ * its first read, so it may be enqueued right after the expert's kernel. */
 ep_status_t ep_combine_recv(ep_handle_t *h, const void *d_y,
                             int64_t y_rank_stride_bytes, const float *d_w_in,
                             int64_t w_rank_stride_bytes, const int32_t *d_idx,
