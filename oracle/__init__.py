@@ -91,8 +91,6 @@ def _declare(L):
         "or_combine_fp8": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
         "or_quant_block_f32": (None, [_P, _I, _P, _P]),
         "or_combine": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
-        "or_combine_tokens": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _I,
-                                   _P, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -282,20 +280,6 @@ def combine(wl, num_tokens, pos, y, w_in, cap):
                      _p(_c(pos, np.int32)), _p(_c(y, np.uint16)),
                      _p(None if w_in is None else _c(w_in, np.float32)),
                      _p(out), _p(out_w))
-    return out, out_w
-
-
-def combine_tokens(wl, pos, y, w_in, cap, tokens):
-    """Combine of the sampled global tokens s*T+t: ([n][H], [n][k] or None)."""
-    H, k = wl.hidden, wl.topk
-    tokens = _c(tokens, np.int32)
-    n = tokens.size
-    out = np.zeros((n, H), np.uint16)
-    out_w = np.zeros((n, k), np.float32) if w_in is not None else None
-    lib().or_combine_tokens(wl.world_size, k, wl.max_tokens_per_rank, H, cap,
-                            _p(_c(pos, np.int32)), _p(_c(y, np.uint16)),
-                            _p(None if w_in is None else _c(w_in, np.float32)),
-                            _p(tokens), n, _p(out), _p(out_w))
     return out, out_w
 
 

@@ -455,22 +455,6 @@ int or_combine(int W, int k, int T, int H, int cap, const int32_t *num_tokens,
     return OR_OK;
 }
 
-/* Combine of a sample of tokens, given as global ids g = s*T + t: row i of
- * out_rows [n][H] (and out_w_rows [n][k]) is token tokens[i]. */
-int or_combine_tokens(int W, int k, int T, int H, int cap, const int32_t *pos,
-                      const uint16_t *y, const float *w_in,
-                      const int32_t *tokens, int n,
-                      uint16_t *out_rows, float *out_w_rows)
-{
-    for (int i = 0; i < n; ++i) {
-        int s = tokens[i] / T, t = tokens[i] % T;
-        combine_token(W, k, T, H, cap, s, t, pos, y, w_in,
-                      out_rows + (int64_t)i * H,
-                      out_w_rows ? out_w_rows + (int64_t)i * k : 0);
-    }
-    return OR_OK;
-}
-
 /* ------------------------------------------- pre-quantised FP8 dispatch */
 
 /* Dispatch of an input that is already quantised (the pages' dispatch takes
