@@ -69,6 +69,9 @@ def parse():
                          "graph of it (per-kernel times always come from eager steps)")
     ap.add_argument("--combine-mode", choices=["gather", "scatter"], default="gather",
                     help="gather combine, or scatter combine through a staging area")
+    ap.add_argument("--flush-l2", action="store_true",
+                    help="write twice the L2 size before every timed step (cold L2; for "
+                         "workloads whose working set fits in L2) and time the steps alone")
     ap.add_argument("--moe-group", type=int, default=0, metavar="GCAP",
                     help="also time the standard-MoE grouping / un-grouping with "
                          "GCAP grouped rows per rank (reported beside the step)")
@@ -355,13 +358,25 @@ def run_ours(args, rank, world, local_rank):
     t_host0 = time.time()
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
+    if args.flush_l2:
+        # cold L2: a write of twice the L2 size before every step, outside
+        # the step's own events; the step times are summed
+        flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size,
+                            dtype=torch.uint8, device=dev)
+        fev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+               for _ in range(args.steps)]
     with torch.cuda.stream(stream):
         start.record(stream)
         for i in range(args.steps):
+            if args.flush_l2:
+                flush.fill_(i & 0xFF)
+                fev[i][0].record(stream)
             if graph is not None:
                 graph.replay()
             else:
                 timed_step()
+            if args.flush_l2:
+                fev[i][1].record(stream)
         stop.record(stream)
     stop.synchronize()
     torch.cuda.synchronize()
@@ -369,6 +384,8 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     t_host1 = time.time()
     total_ms = start.elapsed_time(stop)
+    if args.flush_l2:
+        total_ms = float(sum(e[0].elapsed_time(e[1]) for e in fev))
     with torch.cuda.stream(stream):   # per-kernel split: the same work, eagerly
         for i in range(args.steps):
             step(evs[i])
@@ -389,6 +406,7 @@ def run_ours(args, rank, world, local_rank):
                            y_bytes={"fp32": 4, "bf16": 2, "fp8_e4m3": 1 + 4 / 128}[args.combine_dtype],
                            scatter=args.combine_mode == "scatter")
     step_bytes = ab["dispatch"] + ab["combine"]
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     peak, peak_kind = measured_peak()
     d_ms, c_ms = float(dis.mean()), float(com.mean())
     dominant = "combine" if c_ms >= d_ms else "dispatch"
@@ -552,8 +570,14 @@ def run_ours(args, rank, world, local_rank):
             "workload": workload_text(wl, args),
             "tokens_per_step": N,
             "routed_pairs": P,
-            "l2": "every input and output is larger than L2 (x 470 MB, "
-                  "dispatch out ~2.5 GB, combine in ~2.5 GB); no flush",
+            "l2": ("L2 flushed before every timed step (a write of twice its size), "
+                   "the flush outside the step's events" if args.flush_l2 else
+                   f"no flush: each step moves {step_bytes / 1e6:.0f} MB "
+                   f"({step_bytes / l2_bytes:.1f}x the {l2_bytes / 1e6:.0f} MB L2) between "
+                   "two reads of any input, and the copies use L2 evict-first hints"
+                   if step_bytes >= 2 * l2_bytes else
+                   f"warm L2: the step's {step_bytes / 1e6:.1f} MB fit in the "
+                   f"{l2_bytes / 1e6:.0f} MB L2 (--flush-l2 gives the cold figure)"),
             "parallelism": f"replicas x{world}",
             "step": ("dispatch_send (layout + copy) on stream A, dispatch_recv + "
                      "combine_send on stream B, combine_recv on A" if args.split else
