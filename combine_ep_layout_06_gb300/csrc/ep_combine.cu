@@ -36,9 +36,6 @@ namespace {
 #ifndef EP_COMBINE_UNROLL8
 #define EP_COMBINE_UNROLL8 2       // column vectors in flight per row, <= 8 rows
 #endif
-#ifndef EP_COMBINE_PDL
-#define EP_COMBINE_PDL 1              // launch programmatically after the previous kernel
-#endif
 #ifndef EP_COMBINE_FP8_MIN_BLOCKS
 #define EP_COMBINE_FP8_MIN_BLOCKS 3   // FP8 rows (16-code vectors): <= 80 registers
 #endif
@@ -153,11 +150,13 @@ struct RowVec {
     uint4 b;
 };
 
-template <int YK, bool COHERENT>
+template <int YK, bool COHERENT, bool FEW>
 __device__ __forceinline__ RowVec load_vec(const char *row, int v) {
     RowVec r;
     if constexpr (YK == kYBf16) {
-        r.a = COHERENT ? ld_coherent16(row + (int64_t)v * 16) : ld_stream16(row + (int64_t)v * 16);
+        r.a = COHERENT ? ld_coherent16(row + (int64_t)v * 16)
+                       : (FEW ? ld_stream16_na(row + (int64_t)v * 16)
+                              : ld_stream16(row + (int64_t)v * 16));
     } else {
         r.a = COHERENT ? ld_coherent16(row + (int64_t)v * 32) : ld_stream16(row + (int64_t)v * 32);
         r.b = COHERENT ? ld_coherent16(row + (int64_t)v * 32 + 16)
@@ -176,7 +175,8 @@ __device__ __forceinline__ void add_vec(float acc[8], const RowVec &r) {
     }
 }
 
-template <int MAXD, int U, bool COHERENT, int YK, bool STAGED>
+// FEW: few tokens (the gather is latency-bound): loads not allocated in L1.
+template <int MAXD, int U, bool COHERENT, int YK, bool STAGED, bool FEW = false>
 __global__ void __launch_bounds__(kCombineThreads,
                                   YK == kYFp8 ? EP_COMBINE_FP8_MIN_BLOCKS : EP_COMBINE_MIN_BLOCKS)
 combine_kernel(const CombineParams p) {
@@ -284,7 +284,7 @@ combine_kernel(const CombineParams p) {
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int v = v0 + 32 * u;
-                    if (v < p.nvec) val[u][j] = load_vec<YK, COHERENT>(rows[j], v);
+                    if (v < p.nvec) val[u][j] = load_vec<YK, COHERENT, FEW>(rows[j], v);
                 }
             }
         }
@@ -481,29 +481,25 @@ __global__ void __launch_bounds__(256) identity_expert_kernel(const IdentityPara
     }
 }
 
+// Up to this many tokens (W x T) the bf16 gather takes loads not allocated
+// in L1 (2048 tokens measured faster so; 32 768 slower).
+constexpr int64_t kFewTokens = 4096;
+
 template <int MAXD, int U, bool COH, int YK>
 cudaError_t launch_combine_t(const Config &c, const CombineParams &p,
                              cudaStream_t st) {
     const int64_t tokens = (int64_t)c.W * c.T;
     const int blocks = (int)((tokens + kCombineWarps - 1) / kCombineWarps);
-#if EP_COMBINE_PDL
     if constexpr (YK == kYBf16) {
         if (p.stage)
             return launch_after_previous(combine_kernel<MAXD, U, COH, YK, true>, blocks,
                                          kCombineThreads, 0, st, p);
+        if (!COH && tokens <= kFewTokens)
+            return launch_after_previous(combine_kernel<MAXD, U, COH, YK, false, true>, blocks,
+                                         kCombineThreads, 0, st, p);
     }
     return launch_after_previous(combine_kernel<MAXD, U, COH, YK, false>, blocks, kCombineThreads,
                                  0, st, p);
-#else
-    if constexpr (YK == kYBf16) {
-        if (p.stage) {
-            combine_kernel<MAXD, U, COH, YK, true><<<blocks, kCombineThreads, 0, st>>>(p);
-            return cudaGetLastError();
-        }
-    }
-    combine_kernel<MAXD, U, COH, YK, false><<<blocks, kCombineThreads, 0, st>>>(p);
-    return cudaGetLastError();
-#endif
 }
 
 template <int MAXD, int U, int YK>
