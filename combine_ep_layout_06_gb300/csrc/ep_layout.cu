@@ -50,6 +50,9 @@ layout_kernel(const LayoutParams p) {
     const int warp = threadIdx.x >> 5;
     const int q = blockIdx.x;
     const int g = q * kGroup + warp;
+    // launched programmatically after whatever kernel precedes it on the
+    // stream: the expert ids are complete from here
+    grid_dependency_wait();
     // the copy kernel launched after this one may start now: its CTAs load
     // their rows and then wait for this grid's results
     grid_dependents_may_launch();
@@ -167,8 +170,7 @@ cudaError_t launch_layout(const Config &c, const Workspace &ws,
     p.nch = c.nch; p.G = c.G; p.Q = c.Q; p.cap = c.cap;
     p.publish = publish ? 1 : 0;
     p.nt = nt;
-    layout_kernel<<<c.Q, kLayoutThreads, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_after_previous(layout_kernel, (unsigned)c.Q, (unsigned)kLayoutThreads, 0, st, p);
 }
 
 }  // namespace ep
