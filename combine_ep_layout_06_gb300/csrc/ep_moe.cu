@@ -267,12 +267,13 @@ __global__ void __launch_bounds__(kGroupWarps * 32) moe_group_bulk_kernel(const 
     if (warp == 0) {
         if (lane == 0) {
             const uint32_t bytes = (uint32_t)p.row_bytes;
-            const uint64_t pol = l2_evict_first_policy();
+            const uint64_t pol = 0;   // these copies take no L2 cache hint
             auto issue = [&](int i) {
                 const int st = i % STAGES;
                 mbar_expect_tx(&bar[st], bytes);
-                bulk_load(gstage + (size_t)st * bytes,
-                          seg + p.off_out + ((int64_t)c * kChunk + i) * bytes, bytes, &bar[st], pol);
+                bulk_load<false>(gstage + (size_t)st * bytes,
+                                 seg + p.off_out + ((int64_t)c * kChunk + i) * bytes, bytes,
+                                 &bar[st], pol);
             };
             const int pre = rows < STAGES ? rows : STAGES;
             for (int i = 0; i < pre; ++i) issue(i);
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(kGroupWarps * 32) moe_group_bulk_kernel(const 
                 for (int j = 0; j < p.k; ++j) {
                     const int q = sm.slot[i][j];
                     if (q >= 0 && q < p.gcap)
-                        bulk_store(seg + p.off_xg + (int64_t)q * bytes, src, bytes, pol);
+                        bulk_store<false>(seg + p.off_xg + (int64_t)q * bytes, src, bytes, pol);
                 }
                 bulk_commit();
                 // the stage of row i-1: its stores were committed one group ago
