@@ -353,7 +353,7 @@ dispatch_kernel(const DispatchParams p) {
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
                         const int pv = base + lane + 32 * u;
-                        if (pv < npair) st_stream16(dst + pv, q[u]);
+                        if (pv < npair) st_plain16(dst + pv, q[u]);
                     }
                 }
             }
