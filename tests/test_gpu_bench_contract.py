@@ -1,0 +1,40 @@
+"""The benchmark's JSON line on a GPU: one line with the metric, the whole-job
+value, the roofline of the dominant kernel against the measured peak, the
+CPU baseline (the oracle), the end-to-end figure with its copied bytes,
+sampled clocks and the count of this library's kernel launches."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_bench_line_keys_on_a_small_workload():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "tiny",
+                          "--steps", "5", "--warmup", "3", "--e2e-steps", "3"],
+                         capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-3000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    import bench
+    assert d["metric"] == bench.METRIC and d["unit"] == "tokens/s"
+    assert d["n_gpus"] == 1 and d["steps"] == 5 and d["warmup"] == 3
+    assert d["higher_is_better"] is True and d["scaling"] == "weak"
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["config"]["workload"].startswith("tiny: W=2 logical ranks")
+    r = d["roofline"]
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    c = d["cpu_baseline"]
+    assert c["kind"] == "oracle" and c["cores"] == 1 and c["value"] > 0
+    e = d["e2e"]
+    assert e["value"] > 0 and e["output_check"] == "pass"
+    assert e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert d["gpu_launches"] == 3 * 5
+    assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    assert d["identity_check"] == "pass" and d["device_errors"] == 0
