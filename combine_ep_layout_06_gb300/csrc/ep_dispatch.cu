@@ -23,6 +23,9 @@
 //    stages, one load per source row and one bulk store per destination.
 #include <cuda_fp8.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "ep_device.cuh"
 
 namespace ep {
@@ -538,9 +541,10 @@ cudaError_t launch_dispatch_bulk(const Config &c, const DispatchParams &p, bool 
     // Function attributes are per device: cache the opted-in size and the
     // shared-memory figures per device.
     constexpr int kMaxDevices = 64;
-    static size_t configured[kMaxDevices] = {};
-    static long per_sm[kMaxDevices] = {};
-    static long fixed[kMaxDevices] = {};     // reserved + static shared memory per CTA
+    // (atomics: handles on different host threads may launch at once)
+    static std::atomic<size_t> configured[kMaxDevices];
+    static std::atomic<long> per_sm[kMaxDevices];
+    static std::atomic<long> fixed[kMaxDevices];   // reserved + static shared memory per CTA
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -549,7 +553,7 @@ cudaError_t launch_dispatch_bulk(const Config &c, const DispatchParams &p, bool 
     size_t dyn = (size_t)STAGES * row;
     const size_t per_cta = (size_t)TPC * (size_t)(c.W < c.k ? c.W : c.k) * row;
     if (EP_DISPATCH_BULK_CTAS_PER_SM > 0 && per_cta >= 64 * 1024) {
-        if (per_sm[dev] == 0) {
+        if (per_sm[dev].load(std::memory_order_acquire) == 0) {
             int sm_bytes = 0, reserved = 0;
             cudaFuncAttributes fa;
             if ((e = cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
@@ -558,19 +562,26 @@ cudaError_t launch_dispatch_bulk(const Config &c, const DispatchParams &p, bool 
                                             dev)) != cudaSuccess ||
                 (e = cudaFuncGetAttributes(&fa, dispatch_bulk_kernel<STAGES, TPC>)) != cudaSuccess)
                 return e;
-            fixed[dev] = (long)reserved + (long)fa.sharedSizeBytes;
-            per_sm[dev] = sm_bytes;
+            fixed[dev].store((long)reserved + (long)fa.sharedSizeBytes, std::memory_order_relaxed);
+            per_sm[dev].store(sm_bytes, std::memory_order_release);
         }
         long ctas = (long)(kBulkStreamBytes / row);
         if (ctas < EP_DISPATCH_BULK_CTAS_PER_SM) ctas = EP_DISPATCH_BULK_CTAS_PER_SM;
-        const long share = (per_sm[dev] / ctas - fixed[dev]) & ~127L;
+        const long share = (per_sm[dev].load(std::memory_order_acquire) / ctas -
+                            fixed[dev].load(std::memory_order_relaxed)) &
+                           ~127L;
         if (share > 0 && (size_t)share > dyn) dyn = (size_t)share;
     }
-    if (dyn > configured[dev]) {        // opt in to the dynamic size
-        e = cudaFuncSetAttribute(dispatch_bulk_kernel<STAGES, TPC>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
-        if (e != cudaSuccess) return e;
-        configured[dev] = dyn;
+    if (dyn > configured[dev].load(std::memory_order_acquire)) {   // opt in to the dynamic size
+        // never lower the attribute under a concurrent launch that needs more
+        static std::mutex mu;
+        std::lock_guard<std::mutex> lock(mu);
+        if (dyn > configured[dev].load(std::memory_order_relaxed)) {
+            e = cudaFuncSetAttribute(dispatch_bulk_kernel<STAGES, TPC>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+            if (e != cudaSuccess) return e;
+            configured[dev].store(dyn, std::memory_order_release);
+        }
     }
     return launch_copy(dispatch_bulk_kernel<STAGES, TPC>, c.G * (kChunk / TPC), dyn, after_layout,
                        p, st);

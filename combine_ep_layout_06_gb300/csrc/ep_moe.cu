@@ -24,6 +24,9 @@
 //          order (a rounded multiply, then a rounded add: no contraction).
 #include <cuda_bf16.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "ep_device.cuh"
 
 namespace ep {
@@ -449,16 +452,21 @@ cudaError_t launch_moe_group(const Config &c, const Workspace &ws, cudaStream_t 
     const size_t dyn = (size_t)EP_MOE_GROUP_BULK_STAGES * p.row_bytes;
     if (dyn <= 160 * 1024) {
         constexpr int kMaxDevices = 64;     // function attributes are per device
-        static size_t configured[kMaxDevices] = {};
+        static std::atomic<size_t> configured[kMaxDevices];   // launches may race
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
         if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-        if (dyn > configured[dev]) {
-            e = cudaFuncSetAttribute(moe_group_bulk_kernel<EP_MOE_GROUP_BULK_STAGES>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
-            if (e != cudaSuccess) return e;
-            configured[dev] = dyn;
+        if (dyn > configured[dev].load(std::memory_order_acquire)) {
+            // never lower the attribute under a concurrent launch that needs more
+            static std::mutex mu;
+            std::lock_guard<std::mutex> lock(mu);
+            if (dyn > configured[dev].load(std::memory_order_relaxed)) {
+                e = cudaFuncSetAttribute(moe_group_bulk_kernel<EP_MOE_GROUP_BULK_STAGES>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+                if (e != cudaSuccess) return e;
+                configured[dev].store(dyn, std::memory_order_release);
+            }
         }
         moe_group_bulk_kernel<EP_MOE_GROUP_BULK_STAGES><<<chunks, kGroupWarps * 32, dyn, st>>>(p);
         return cudaGetLastError();
