@@ -537,3 +537,44 @@ def test_repeated_steps_alternating_inputs_stay_exact():
             n = int(inp.num_tokens[s])
             assert np.array_equal(got[s, :n], ref["combined"][s, :n]), (i, s)
     assert op.get_error() == (0, 0)
+
+
+def test_handles_on_two_host_threads():
+    """Two handles with different row sizes driven from two host threads at
+    once, each on its own stream: both results exact (the per-device launch
+    settings they share are raised, never lowered, under concurrency)."""
+    import threading
+    cases = []
+    for H in (7168, 2048):
+        wl = gen.WORKLOADS["dsv3"].scaled(96, hidden=H)
+        inp = gen.make_inputs(wl, seed=H)
+        cases.append((wl, inp, oracle.run_all(inp, cap=wl.world_size * wl.max_tokens_per_rank)))
+    errors = []
+
+    def worker(wl, inp, ref):
+        try:
+            torch.cuda.set_device(0)
+            op = make_op(wl)
+            x, w, idx = to_device(inp)
+            st = torch.cuda.Stream()
+            out = torch.empty((wl.world_size, wl.max_tokens_per_rank, wl.hidden),
+                              dtype=torch.bfloat16, device="cuda")
+            with torch.cuda.stream(st):
+                for _ in range(20):
+                    op.dispatch(x, w, None, idx, stream=st)
+                    op.identity_expert(stream=st)
+                    op.combine(weights=op.out_w, out=out, stream=st)
+            st.synchronize()
+            if not np.array_equal(bits(out), ref["combined"]):
+                errors.append(f"H={wl.hidden}: combined differs")
+            if op.get_error(st) != (0, 0):
+                errors.append(f"H={wl.hidden}: device error")
+        except Exception as e:   # reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=c) for c in cases]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
