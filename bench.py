@@ -574,7 +574,8 @@ def run_ours(args, rank, world, local_rank):
                    "the flush outside the step's events" if args.flush_l2 else
                    f"no flush: each step moves {step_bytes / 1e6:.0f} MB "
                    f"({step_bytes / l2_bytes:.1f}x the {l2_bytes / 1e6:.0f} MB L2) between "
-                   "two reads of any input, and the copies use L2 evict-first hints"
+                   "two reads of any input (every input and output is read or written once "
+                   "per step)"
                    if step_bytes >= 2 * l2_bytes else
                    f"warm L2: the step's {step_bytes / 1e6:.1f} MB fit in the "
                    f"{l2_bytes / 1e6:.0f} MB L2 (--flush-l2 gives the cold figure)"),
