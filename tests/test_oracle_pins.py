@@ -671,3 +671,39 @@ def test_fp8_combine_payload_matches_bruteforce(fp8):
             continue
         assert np.all(np.abs(o[s_, :n] - x[s_, :n]) <= np.abs(x[s_, :n]) * 0.2 +
                       np.abs(x[s_, :n]).max() * 2.0 ** -9)
+
+
+def test_input_recipe_properties_at_full_size():
+    """The seeded synthetic inputs have the recipe's stated properties at the
+    benchmark sizes: distinct top-k experts per token, weights summing to 1
+    within fp32, E[|D|] of uniform routing equal to its closed form
+    W * (1 - C(E-Er, k) / C(E, k)), Zipf routing visibly skewed across experts
+    and ranks,
+    Mixtral routing confined to experts 0-5, and x with the stated sigma."""
+    from math import comb
+    for name in ["dsv3", "dsv3_fp8_zipf", "mixtral"]:
+        wl = gen.WORKLOADS[name]
+        inp = gen.make_inputs(wl)
+        W, E, k, Er = wl.world_size, wl.num_experts, wl.topk, wl.experts_per_rank
+        idx = inp.indices.reshape(-1, k)
+        srt = np.sort(idx, axis=1)
+        assert np.all(srt[:, 1:] != srt[:, :-1]), name           # distinct experts
+        assert np.all((idx >= 0) & (idx < E))
+        assert np.allclose(inp.weights.sum(axis=-1), 1.0, atol=1e-6), name
+        ranks = idx // Er
+        nd = np.array([len(set(r)) for r in ranks.tolist()])
+        per_rank = np.bincount(np.concatenate([np.unique(r) for r in ranks.tolist()]),
+                               minlength=W)
+        if name == "dsv3":
+            exact = W * (1 - comb(E - Er, k) / comb(E, k))
+            assert abs(nd.mean() - exact) < 0.02, (nd.mean(), exact)
+            assert per_rank.max() / per_rank.mean() < 1.02
+        if name == "dsv3_fp8_zipf":
+            assert per_rank.max() / per_rank.mean() > 1.3          # skewed ranks
+            cnt = np.bincount(idx.ravel(), minlength=E)
+            assert np.sort(cnt)[-1] > 20 * np.median(cnt)          # a few hot experts
+        if name == "mixtral":
+            assert idx.max() <= 5 and np.all(nd == 2)
+        x = (inp.x_bits[0, :512].astype(np.uint32) << 16).view(np.float32)
+        sigma = np.sqrt(2.0) if name == "mixtral" else 1.0
+        assert abs(x.std() / sigma - 1) < 0.01, (name, x.std())
