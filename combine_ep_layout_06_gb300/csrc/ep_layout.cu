@@ -110,6 +110,35 @@ layout_kernel(const LayoutParams p) {
     const int q0 = min(p.Q, lane * per);
     const int q1 = min(p.Q, q0 + per);
     for (int r = warp; r < p.W; r += kLayoutWarps) {
+        if (per <= kScanBatch) {   // warp-uniform: the shuffles need every lane
+            // one batch per lane (up to 256 groups): the totals stay in
+            // registers between the sum and the prefix, one read of L2
+            int v[kScanBatch];
+#pragma unroll
+            for (int i = 0; i < kScanBatch; ++i)
+                v[i] = (q0 + i < q1) ? __ldcg(p.group_tot + (int64_t)(q0 + i) * p.W + r) : 0;
+            int sum = 0;
+#pragma unroll
+            for (int i = 0; i < kScanBatch; ++i) sum += v[i];
+            int incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int x = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += x;
+            }
+            int run = incl - sum;
+#pragma unroll
+            for (int i = 0; i < kScanBatch; ++i) {
+                if (q0 + i < q1) p.group_base[(int64_t)(q0 + i) * p.W + r] = run;
+                run += v[i];
+            }
+            if (lane == 31) {
+                p.group_base[(int64_t)p.Q * p.W + r] = incl;
+                if (incl > p.cap) set_error(p.words, EP_DEVERR_CAPACITY);
+                if (p.publish) p.recv_count[r] = incl;
+            }
+            continue;
+        }
         int sum = 0;
         for (int b0 = q0; b0 < q1; b0 += kScanBatch) {
             int v[kScanBatch];
