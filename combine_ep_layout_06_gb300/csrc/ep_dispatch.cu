@@ -53,7 +53,7 @@ namespace {
 #define EP_DISPATCH_FP8_PREFETCH 1     // FP8: load the next element pair while quantising
 #endif
 #ifndef EP_FP8_RECIP_QUOT
-#define EP_FP8_RECIP_QUOT 1            // FP8: quotient by reciprocal + one FMA correction
+#define EP_FP8_RECIP_QUOT 1            // FP8: quotients by reciprocal + one FMA correction
 #endif
 #ifndef EP_DISPATCH_PDL
 #define EP_DISPATCH_PDL 1              // launch the copy programmatically after the layout
@@ -207,11 +207,29 @@ __device__ __forceinline__ uint32_t quant4(const float *f, float scale) {
 // for every quotient large enough to give a nonzero code, and the E4M3 code
 // of the result equals that of the IEEE quotient for every bf16 x (checked
 // exhaustively over all bf16 x and block maxima); smaller scales divide.  The
-// sign of x is put back so that a quotient that is zero keeps the sign of x.
+// residual is formed negated, q0*scale - x (the same magnitude: RN is
+// symmetric), and applied with -r, so that for x = +-0 the sums of zeros
+// keep the sign of x (the code of -0 is 0x80) with no sign fix-up.
 __device__ __forceinline__ float quot_recip(float x, float scale, float r) {
     const float q0 = __fmul_rn(x, r);
-    const float res = __fmaf_rn(-q0, scale, x);
-    return copysignf(__fmaf_rn(res, r, q0), x);
+    const float nres = __fmaf_rn(q0, scale, -x);
+    return __fmaf_rn(nres, -r, q0);
+}
+
+// fl32(a / 448) for a block maximum a > 0 (a bf16 magnitude): the product
+// with RN(1/448) and the same one-FMA correction.  Equal to the IEEE
+// quotient for every finite non-negative bf16 a (checked exhaustively in
+// exact rational arithmetic); a = inf gives inf.
+__device__ __forceinline__ float block_scale(float a) {
+#if EP_FP8_RECIP_QUOT
+    constexpr float kInv448 = 0x1.24924ap-9f;   // RN(1/448)
+    const float q0 = __fmul_rn(a, kInv448);
+    const float e = __fmaf_rn(-q0, 448.0f, a);
+    const float q = __fmaf_rn(e, kInv448, q0);
+    return a <= 0x1.fffffep127f ? q : a;
+#else
+    return a / 448.0f;
+#endif
 }
 
 __device__ __forceinline__ uint32_t quant4_recip(const float *f, float scale, float r) {
@@ -328,7 +346,7 @@ dispatch_kernel(const DispatchParams p) {
                     float scale = 0.f;
                     q[u] = make_uint4(0u, 0u, 0u, 0u);
                     if (a != 0.f) {
-                        scale = a / 448.0f;
+                        scale = block_scale(a);
 #if EP_FP8_RECIP_QUOT
                         if (scale >= 0x1p-90f) {   // the same for the block's 8 lanes
                             const float r = __frcp_rn(scale);
