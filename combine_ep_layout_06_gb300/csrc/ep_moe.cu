@@ -35,6 +35,9 @@ namespace {
 #ifndef EP_MOE_GROUP_BULK_STAGES
 #define EP_MOE_GROUP_BULK_STAGES 4    // grouping by TMA bulk copies (0: register path)
 #endif
+#ifndef EP_MOE_GROUP_EARLY_LOADS
+#define EP_MOE_GROUP_EARLY_LOADS 1    // grouping: row loads issued before the slot scan
+#endif
 
 constexpr int kMoeWarps = 8;
 constexpr int kGroupWarps = 4;
@@ -257,29 +260,37 @@ __global__ void __launch_bounds__(kGroupWarps * 32) moe_group_bulk_kernel(const 
     const int n_r = rank_rows(p, r);
     char *seg = p.seg0 + (int64_t)r * p.seg_stride;
     const int rows = max(0, min(kChunk, n_r - c * kChunk));
+    const uint32_t bytes = (uint32_t)p.row_bytes;
+    const uint64_t pol = 0;   // these copies take no L2 cache hint
+    auto issue = [&](int i) {
+        const int st = i % STAGES;
+        mbar_expect_tx(&bar[st], bytes);
+        bulk_load<false>(gstage + (size_t)st * bytes,
+                         seg + p.off_out + ((int64_t)c * kChunk + i) * bytes, bytes,
+                         &bar[st], pol);
+    };
+    const int pre = rows < STAGES ? rows : STAGES;
     if (warp == 0) {
-        group_slots(p, r, c, n_r, seg, sm);
         if (lane == 0) {
             for (int i = 0; i < STAGES; ++i) mbar_init(&bar[i], 1);
             mbar_init_fence();
+#if EP_MOE_GROUP_EARLY_LOADS
+            // the rows do not depend on the slots: start them first
+            // (990 against 994 us on the DeepSeek-V3 shape)
+            for (int i = 0; i < pre; ++i) issue(i);
+#endif
         }
+        __syncwarp();
+        group_slots(p, r, c, n_r, seg, sm);
     }
     __syncthreads();
     if (rows == 0) return;
 
     if (warp == 0) {
         if (lane == 0) {
-            const uint32_t bytes = (uint32_t)p.row_bytes;
-            const uint64_t pol = 0;   // these copies take no L2 cache hint
-            auto issue = [&](int i) {
-                const int st = i % STAGES;
-                mbar_expect_tx(&bar[st], bytes);
-                bulk_load<false>(gstage + (size_t)st * bytes,
-                                 seg + p.off_out + ((int64_t)c * kChunk + i) * bytes, bytes,
-                                 &bar[st], pol);
-            };
-            const int pre = rows < STAGES ? rows : STAGES;
+#if !EP_MOE_GROUP_EARLY_LOADS
             for (int i = 0; i < pre; ++i) issue(i);
+#endif
             int issued = pre;
             bool ok = true;
             for (int i = 0; i < rows; ++i) {
