@@ -5,9 +5,10 @@
 // the correctness harness.
 //
 // Definition (ROCm MORI "Communication APIs", MORI-EP, "EpDispatchCombineOp
-// methods": combine(input, weights, indices) -> (output, weights), "combine
-// expert outputs back"; combine_send()/combine_recv(); and the "AsyncLL v2
-// SDMA overlap" section for the split receive): out[s][t] = bf16_rne(
+// methods": combine(input, weights, indices) -> (output, weights), which
+// returns the experts' results to the source tokens; combine_send() /
+// combine_recv(); and the "AsyncLL v2 SDMA overlap" section for the split
+// receive): out[s][t] = bf16_rne(
 // +0.0f + y_r0[p0] + y_r1[p1] + ...) over r in D(s,t) ascending, each '+' an
 // fp32 add.  The expert rows are bf16, fp32, or E4M3 codes with one fp32
 // scale per 128 elements (each element then enters as fl32(value(q)*scale)).

@@ -209,9 +209,10 @@ class EpDispatchCombineOp:
 
     def dispatch(self, input, weights, scales=None, indices=None,
                  num_tokens: Optional[Sequence[int]] = None, stream=None):
-        """Route tokens to expert ranks.  Returns (output, weights, scales,
-        indices, recv_count): per-rank views [W][cap][...] into the receive
-        segments (valid until the next dispatch / reset) and recv_count [W].
+        """Send each token to the ranks that hold its experts.  Returns
+        (output, weights, scales, indices, recv_count): per-rank views
+        [W][cap][...] into the receive segments (valid until the next
+        dispatch / reset) and recv_count [W].
         Rows p >= recv_count[r] of rank r are unspecified."""
         self._check_inputs(input, weights, indices, scales)
         check(self.L.ep_dispatch(self.h, _ptr(input), _ptr(weights),
@@ -273,8 +274,9 @@ class EpDispatchCombineOp:
 
     def combine(self, input=None, weights=None, indices=None, out=None,
                 out_weights=None, stream=None):
-        """Combine expert outputs back.  input: None for the registered
-        combine buffer, else bf16 [W][cap][H] expert rows per rank.  Returns
+        """Bring the experts' results back to the source tokens.  input: None
+        for the registered combine buffer, else bf16 [W][cap][H] expert rows
+        per rank.  Returns
         (output [W][T][H] bf16, weights [W][T][k] fp32 or None)."""
         return self._combine_call(self.L.ep_combine, input, weights, indices,
                                   out, out_weights, stream, "ep_combine")

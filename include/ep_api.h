@@ -6,10 +6,10 @@
  * page, section "MORI-EP (Expert Parallelism)", table "EpDispatchCombineOp
  * methods":
  *   dispatch(input, weights, scales, indices)
- *       -> (output, weights, scales, indices, recv_count)   "route tokens to
- *          expert ranks"
- *   combine(input, weights, indices) -> (output, weights)    "combine expert
- *          outputs back"
+ *       -> (output, weights, scales, indices, recv_count)   sends each token
+ *          to the ranks that hold its experts
+ *   combine(input, weights, indices) -> (output, weights)    brings the
+ *          experts' results back to the source tokens
  *   dispatch_send()/dispatch_recv(), combine_send()/combine_recv()  split
  *          phases for overlapping independent work
  *   reset(), get_dispatch_src_token_pos(),
@@ -201,8 +201,8 @@ ep_status_t ep_layout(ep_handle_t *h, const int32_t *d_idx,
  *  - d_scales == NULL: d_x is [W][T][H] bf16; with an FP8 dispatch_dtype
  *    every row is quantised on the way (fused per-128-element E4M3);
  *  - d_scales != NULL (FP8 dispatch_dtype only; the pages' dispatch takes
- *    `scales` beside `input` and "can carry already-quantized FP8
- *    payloads"): d_x is [W][T][H] E4M3 codes and d_scales [W][T][H/128]
+ *    `scales` beside `input`, and a backend may pass FP8 input that is
+ *    quantised already): d_x is [W][T][H] E4M3 codes and d_scales [W][T][H/128]
  *    fp32 block scales, both copied unchanged.
  * Inputs must stay unchanged until the receive phase has been enqueued.
  * The copy kernel is launched as a programmatic dependent of the layout

@@ -458,8 +458,8 @@ int or_combine(int W, int k, int T, int H, int cap, const int32_t *num_tokens,
 /* ------------------------------------------- pre-quantised FP8 dispatch */
 
 /* Dispatch of an input that is already quantised (the pages' dispatch takes
- * `scales` next to `input`; the HIP backend "can carry already-quantized
- * FP8 payloads"): the E4M3 codes x8[s][t][0..H) and the block scales
+ * `scales` next to `input`; the HIP backend accepts FP8 input
+ * that is quantised already): the E4M3 codes x8[s][t][0..H) and the block scales
  * sc[s][t][0..H/128) of each present token are copied unchanged to every
  * destination slot p = pos[s][t][r] < cap, with the weights, ids and
  * src_pos as in or_dispatch.  out uint8 [W][cap][H], out_scales
