@@ -38,8 +38,10 @@
  *  - dispatch: row p = pos[s][t][r] of rank r receives x[s][t] (bf16 bits,
  *    or FP8 E4M3 codes plus one fp32 scale per 128 elements with
  *    scale = fl32(amax/448) and q = RNE-satfinite(fl32(x/scale)); an
- *    all-zero block gives scale 0 and codes 0x00), all k weights and all k
- *    expert ids unchanged, and src_pos = s*T + t.
+ *    all-zero block gives scale 0 and codes 0x00; the quantised input is
+ *    taken to be finite: a block holding an infinity or a NaN gets an
+ *    unspecified scale and codes), all k weights and all k expert ids
+ *    unchanged, and src_pos = s*T + t.
  *  - combine: out[s][t] = bf16_rne( fp32 sum over r in D(s,t), r ascending,
  *    starting from +0.0f, of y_r[pos[s][t][r]] ); out_w the same ordered
  *    fp32 sum of the expert-side weight rows.  No weighting is applied.
