@@ -117,6 +117,7 @@ SIGNATURES = {
     "ep_moe_group": (_S, [_P, _P]),
     "ep_moe_outputs": (_S, [_P, ctypes.POINTER(EpMoeOutC)]),
     "ep_moe_ungroup": (_S, [_P, _P, _I64, _P]),
+    "ep_test_fp8_quotient_check": (_S, [_P, _P]),
     "ep_layout_noalloc": (_S, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
 }
 

@@ -50,11 +50,15 @@ def up_to_date() -> bool:
 
 
 def build(force: bool = False, ptxas_verbose: bool = False) -> str:
+    """EP_NVTX=1 in the environment compiles NVTX ranges around the entry
+    points in (for timelines and ncu range filters); they are off otherwise."""
     if not force and not ptxas_verbose and up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    if os.environ.get("EP_NVTX", "0") not in ("", "0"):
+        extra.append("-DEP_NVTX=1")
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")

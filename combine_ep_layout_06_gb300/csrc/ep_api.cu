@@ -14,6 +14,7 @@ using namespace ep;
 namespace {
 
 constexpr size_t kAlign = 256;
+constexpr int kMaxHidden = 1 << 24;
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 bool aligned(const void *p, size_t a) {
@@ -33,7 +34,8 @@ ep_status_t make_config(const ep_config_t *in, Config *c) {
     if (W < 1 || W > EP_MAX_WORLD) return EP_ERR_INVALID_ARGS;
     if (E < W || E % W != 0) return EP_ERR_INVALID_ARGS;
     if (k < 1 || k > EP_MAX_TOPK) return EP_ERR_INVALID_ARGS;
-    if (H < 8 || H % 8 != 0) return EP_ERR_INVALID_ARGS;
+    // H <= 2^24 keeps a row's byte count (up to 4 H for fp32 rows) in an int
+    if (H < 8 || H % 8 != 0 || H > kMaxHidden) return EP_ERR_INVALID_ARGS;
     if (T < 1) return EP_ERR_INVALID_ARGS;
     if (in->dispatch_dtype != EP_DT_BF16 && in->dispatch_dtype != EP_DT_FP8_E4M3)
         return EP_ERR_INVALID_ARGS;
@@ -185,6 +187,7 @@ ep_status_t ep_workspace_size(const ep_config_t *cfg, size_t *bytes) {
 
 ep_status_t ep_create(const ep_config_t *cfg, void *d_workspace, size_t bytes,
                       ep_handle_t **out) {
+    EP_RANGE("ep_create");
     if (!out || !d_workspace || !aligned(d_workspace, kAlign))
         return EP_ERR_INVALID_ARGS;
     *out = nullptr;
@@ -206,6 +209,11 @@ ep_status_t ep_create(const ep_config_t *cfg, void *d_workspace, size_t bytes,
     if (st == EP_SUCCESS)
         st = gpu(h, cudaEventCreateWithFlags(&h->ev_combine_sent, cudaEventDisableTiming),
                  "cudaEventCreate");
+    // one pinned host word for ep_get_error's stream-ordered read
+    if (st == EP_SUCCESS)
+        st = gpu(h, cudaHostAlloc(reinterpret_cast<void **>(&h->h_err), sizeof(uint32_t),
+                                  cudaHostAllocDefault),
+                 "cudaHostAlloc");
     // zero the counters, flags and error word (everything before chunk_local)
     if (st == EP_SUCCESS)
         st = gpu(h, cudaMemset(ws.words, 0,
@@ -228,15 +236,18 @@ ep_status_t ep_create(const ep_config_t *cfg, void *d_workspace, size_t bytes,
 }
 
 ep_status_t ep_destroy(ep_handle_t *h) {
+    EP_RANGE("ep_destroy");
     if (!h) return EP_ERR_INVALID_ARGS;
     if (h->ev_dispatch_sent) cudaEventDestroy(h->ev_dispatch_sent);
     if (h->ev_combine_sent) cudaEventDestroy(h->ev_combine_sent);
+    if (h->h_err) cudaFreeHost(h->h_err);
     delete h;
     return EP_SUCCESS;
 }
 
 ep_status_t ep_layout(ep_handle_t *h, const int32_t *d_idx,
                       const int32_t *h_num_tokens, void *stream) {
+    EP_RANGE("ep_layout");
     if (!h || !d_idx || !aligned(d_idx, 4)) return EP_ERR_INVALID_ARGS;
     TokenCounts nt;
     if (!read_counts(h, h_num_tokens, &nt)) return EP_ERR_INVALID_ARGS;
@@ -288,13 +299,18 @@ static ep_status_t dispatch_send_impl(ep_handle_t *h, const void *d_x,
 ep_status_t ep_dispatch_send(ep_handle_t *h, const void *d_x, const float *d_w,
                              const float *d_scales, const int32_t *d_idx,
                              const int32_t *h_num_tokens, void *stream) {
+    EP_RANGE("ep_dispatch_send");
     ep_status_t s = check_dispatch_args(h, d_x, d_w, d_scales, d_idx);
     if (s != EP_SUCCESS) return s;
     TokenCounts nt;
     if (!read_counts(h, h_num_tokens, &nt)) return EP_ERR_INVALID_ARGS;
     if (h->dispatch_pending) return EP_ERR_BAD_STATE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    s = dispatch_send_impl(h, d_x, d_w, d_scales, d_idx, nt, true, false, st);
+    // Without early notification the layout kernel produces recv_count
+    // itself and the receive phase is stream order alone; with it, the
+    // receive step checks the ready flags and then writes the count.
+    s = dispatch_send_impl(h, d_x, d_w, d_scales, d_idx, nt, true,
+                           !h->cfg.early_notify, st);
     if (s != EP_SUCCESS) return s;
     s = gpu(h, cudaEventRecord(h->ev_dispatch_sent, st), "cudaEventRecord");
     if (s != EP_SUCCESS) return s;
@@ -306,6 +322,7 @@ ep_status_t ep_dispatch_send_replay(ep_handle_t *h, const void *d_x,
                                     const float *d_w, const float *d_scales,
                                     const int32_t *d_idx,
                                     const int32_t *h_num_tokens, void *stream) {
+    EP_RANGE("ep_dispatch_send_replay");
     ep_status_t s = check_dispatch_args(h, d_x, d_w, d_scales, d_idx);
     if (s != EP_SUCCESS) return s;
     TokenCounts nt;
@@ -322,16 +339,18 @@ ep_status_t ep_dispatch_send_replay(ep_handle_t *h, const void *d_x,
 }
 
 ep_status_t ep_dispatch_recv(ep_handle_t *h, void *stream) {
+    EP_RANGE("ep_dispatch_recv");
     if (!h) return EP_ERR_INVALID_ARGS;
     if (!h->dispatch_pending) return EP_ERR_BAD_STATE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     ep_status_t s = gpu(h, cudaStreamWaitEvent(st, h->ev_dispatch_sent, 0),
                         "cudaStreamWaitEvent");
     if (s != EP_SUCCESS) return s;
-    s = gpu(h, launch_dispatch_recv(h->cfg, h->ws, h->cfg.early_notify,
-                                    h->dispatch_epoch, st),
-            "dispatch_recv");
-    if (s != EP_SUCCESS) return s;
+    if (h->cfg.early_notify) {
+        s = gpu(h, launch_dispatch_recv(h->cfg, h->ws, true, h->dispatch_epoch, st),
+                "dispatch_recv");
+        if (s != EP_SUCCESS) return s;
+    }
     h->dispatch_pending = false;
     return EP_SUCCESS;
 }
@@ -339,6 +358,7 @@ ep_status_t ep_dispatch_recv(ep_handle_t *h, void *stream) {
 ep_status_t ep_dispatch(ep_handle_t *h, const void *d_x, const float *d_w,
                         const float *d_scales, const int32_t *d_idx,
                         const int32_t *h_num_tokens, void *stream) {
+    EP_RANGE("ep_dispatch");
     ep_status_t s = check_dispatch_args(h, d_x, d_w, d_scales, d_idx);
     if (s != EP_SUCCESS) return s;
     TokenCounts nt;
@@ -398,8 +418,12 @@ ep_status_t ep_get_combine_input_scales(const ep_handle_t *h, float **d_ptr,
 }
 
 ep_status_t ep_combine_send(ep_handle_t *h, void *stream) {
+    EP_RANGE("ep_combine_send");
     if (!h) return EP_ERR_INVALID_ARGS;
-    if (!h->layout_valid || h->combine_pending) return EP_ERR_BAD_STATE;
+    // the dispatch's receive phase must be enqueued first: it orders the
+    // expert side after the send's layout and copy
+    if (!h->layout_valid || h->dispatch_pending || h->combine_pending)
+        return EP_ERR_BAD_STATE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (h->cfg.scatter) {
         const ep_status_t s = gpu(h, launch_scatter_send(h->cfg, h->ws, st), "scatter_send");
@@ -462,6 +486,7 @@ ep_status_t ep_combine_recv(ep_handle_t *h, const void *d_y,
                             int64_t y_rank_stride_bytes, const float *d_w_in,
                             int64_t w_rank_stride_bytes, const int32_t *d_idx,
                             void *d_out, float *d_out_w, void *stream) {
+    EP_RANGE("ep_combine_recv");
     if (!h) return EP_ERR_INVALID_ARGS;
     CombineArgs a;
     ep_status_t s = combine_args(h, d_y, y_rank_stride_bytes, d_w_in,
@@ -486,12 +511,14 @@ ep_status_t ep_combine(ep_handle_t *h, const void *d_y, int64_t y_rank_stride_by
                        const float *d_w_in, int64_t w_rank_stride_bytes,
                        const int32_t *d_idx, void *d_out, float *d_out_w,
                        void *stream) {
+    EP_RANGE("ep_combine");
     if (!h) return EP_ERR_INVALID_ARGS;
     CombineArgs a;
     ep_status_t s = combine_args(h, d_y, y_rank_stride_bytes, d_w_in,
                                  w_rank_stride_bytes, d_idx, d_out, d_out_w, &a);
     if (s != EP_SUCCESS) return s;
-    if (!h->layout_valid || h->combine_pending) return EP_ERR_BAD_STATE;
+    if (!h->layout_valid || h->dispatch_pending || h->combine_pending)
+        return EP_ERR_BAD_STATE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (h->cfg.scatter) {
         s = gpu(h, launch_scatter_send(h->cfg, h->ws, st), "scatter_send");
@@ -514,6 +541,7 @@ ep_status_t ep_combine(ep_handle_t *h, const void *d_y, int64_t y_rank_stride_by
 }
 
 ep_status_t ep_moe_group(ep_handle_t *h, void *stream) {
+    EP_RANGE("ep_moe_group");
     if (!h) return EP_ERR_INVALID_ARGS;
     if (h->cfg.gcap <= 0) return EP_ERR_INVALID_ARGS;
     if (!h->layout_valid || h->dispatch_pending) return EP_ERR_BAD_STATE;
@@ -543,6 +571,7 @@ ep_status_t ep_moe_outputs(const ep_handle_t *h, ep_moe_out_t *o) {
 
 ep_status_t ep_moe_ungroup(ep_handle_t *h, const void *d_yg, int64_t yg_stride,
                            void *stream) {
+    EP_RANGE("ep_moe_ungroup");
     if (!h) return EP_ERR_INVALID_ARGS;
     const Config &c = h->cfg;
     if (c.gcap <= 0 || c.y_f32 || c.y_fp8) return EP_ERR_INVALID_ARGS;
@@ -563,6 +592,7 @@ ep_status_t ep_moe_ungroup(ep_handle_t *h, const void *d_yg, int64_t yg_stride,
 }
 
 ep_status_t ep_reset(ep_handle_t *h, void *stream) {
+    EP_RANGE("ep_reset");
     if (!h) return EP_ERR_INVALID_ARGS;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const ep_status_t s = gpu(
@@ -582,18 +612,21 @@ ep_status_t ep_reset(ep_handle_t *h, void *stream) {
 }
 
 ep_status_t ep_get_error(ep_handle_t *h, uint32_t *mask, void *stream) {
+    EP_RANGE("ep_get_error");
     if (!h || !mask) return EP_ERR_INVALID_ARGS;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    uint32_t word = 0;
-    ep_status_t s = gpu(h, cudaStreamSynchronize(st), "cudaStreamSynchronize");
+    // Stream-ordered read and clear of the word, then a wait for this stream
+    // alone (work on other streams keeps running).  The read lands in the
+    // handle's pinned host word.
+    ep_status_t s = gpu(h, cudaMemcpyAsync(h->h_err, h->ws.words + kWordErr, 4,
+                                           cudaMemcpyDeviceToHost, st),
+                        "cudaMemcpyAsync");
     if (s != EP_SUCCESS) return s;
-    s = gpu(h, cudaMemcpy(&word, h->ws.words + kWordErr, 4, cudaMemcpyDeviceToHost),
-            "cudaMemcpy");
+    s = gpu(h, cudaMemsetAsync(h->ws.words + kWordErr, 0, 4, st), "cudaMemsetAsync");
     if (s != EP_SUCCESS) return s;
-    s = gpu(h, cudaMemset(h->ws.words + kWordErr, 0, 4), "cudaMemset");
+    s = gpu(h, cudaStreamSynchronize(st), "cudaStreamSynchronize");
     if (s != EP_SUCCESS) return s;
-    s = gpu(h, cudaDeviceSynchronize(), "cudaDeviceSynchronize");
-    if (s != EP_SUCCESS) return s;
+    const uint32_t word = *h->h_err;
     *mask = word;
     if (word & EP_DEVERR_BAD_INDEX) return EP_ERR_BAD_INDEX;
     if (word & EP_DEVERR_CAPACITY) return EP_ERR_CAPACITY;
@@ -604,6 +637,7 @@ ep_status_t ep_get_error(ep_handle_t *h, uint32_t *mask, void *stream) {
 
 ep_status_t ep_test_identity_expert(ep_handle_t *h, void *d_y,
                                     int64_t y_rank_stride_bytes, void *stream) {
+    EP_RANGE("ep_test_identity_expert");
     if (!h) return EP_ERR_INVALID_ARGS;
     if (!h->layout_valid) return EP_ERR_BAD_STATE;
     const int64_t row_bytes = (int64_t)h->cfg.cap * h->cfg.H * (h->cfg.y_f32 ? 4 : 2);
@@ -620,6 +654,15 @@ ep_status_t ep_test_identity_expert(ep_handle_t *h, void *d_y,
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return gpu(h, launch_identity_expert(h->cfg, h->ws, y, ys, st), "identity_expert");
+}
+
+ep_status_t ep_test_fp8_quotient_check(uint64_t *d_counts, void *stream) {
+    EP_RANGE("ep_test_fp8_quotient_check");
+    if (!d_counts || !aligned(d_counts, 8)) return EP_ERR_INVALID_ARGS;
+    return gpu(nullptr,
+               launch_fp8_quotient_check(reinterpret_cast<unsigned long long *>(d_counts),
+                                         static_cast<cudaStream_t>(stream)),
+               "fp8_quotient_check");
 }
 
 }  // extern "C"

@@ -46,6 +46,9 @@ namespace {
 #ifndef EP_COMBINE_FP8_UNROLL8
 #define EP_COMBINE_FP8_UNROLL8 1      // 16-code vectors in flight per row, <= 8 rows
 #endif
+#ifndef EP_COMBINE_FP8_PAIRS
+#define EP_COMBINE_FP8_PAIRS 0        // FP8 rows: 0 scalar, 1 two-wide adds, 2 two-wide products too
+#endif
 
 constexpr int kCombineWarps = EP_COMBINE_WARPS;
 constexpr int kCombineThreads = kCombineWarps * 32;
@@ -108,6 +111,17 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
     return __half22float2(__half2(h));
 }
 
+// Two-wide fp32 multiply: each half is the IEEE round-to-nearest product.
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 // acc += fl32(value(q) * scale) for 16 codes (a rounded multiply, then a
 // rounded add); acc[i] holds elements 2i, 2i+1.
 __device__ __forceinline__ void add_fp8x16(float2 acc[8], const uint4 &q, float scale) {
@@ -116,10 +130,21 @@ __device__ __forceinline__ void add_fp8x16(float2 acc[8], const uint4 &q, float 
     for (int i = 0; i < 4; ++i) {
         const float2 lo = e4m3x2_to_float2(w[i] & 0xffffu);
         const float2 hi = e4m3x2_to_float2(w[i] >> 16);
+#if EP_COMBINE_FP8_PAIRS == 0
         acc[2 * i].x = __fadd_rn(acc[2 * i].x, __fmul_rn(lo.x, scale));
         acc[2 * i].y = __fadd_rn(acc[2 * i].y, __fmul_rn(lo.y, scale));
         acc[2 * i + 1].x = __fadd_rn(acc[2 * i + 1].x, __fmul_rn(hi.x, scale));
         acc[2 * i + 1].y = __fadd_rn(acc[2 * i + 1].y, __fmul_rn(hi.y, scale));
+#elif EP_COMBINE_FP8_PAIRS == 1
+        acc[2 * i] = add2_rn(acc[2 * i], make_float2(__fmul_rn(lo.x, scale),
+                                                     __fmul_rn(lo.y, scale)));
+        acc[2 * i + 1] = add2_rn(acc[2 * i + 1], make_float2(__fmul_rn(hi.x, scale),
+                                                             __fmul_rn(hi.y, scale)));
+#else
+        const float2 s2 = make_float2(scale, scale);
+        acc[2 * i] = add2_rn(acc[2 * i], mul2_rn(lo, s2));
+        acc[2 * i + 1] = add2_rn(acc[2 * i + 1], mul2_rn(hi, s2));
+#endif
     }
 }
 

@@ -46,6 +46,9 @@ namespace {
 #ifndef EP_DISPATCH_BULK_CTAS_PER_SM
 #define EP_DISPATCH_BULK_CTAS_PER_SM 2 // resident bulk CTAs per SM (0: no cap)
 #endif
+#ifndef EP_DISPATCH_BULK_CAP_MIN_WAVES
+#define EP_DISPATCH_BULK_CAP_MIN_WAVES 0 // cap residency only for grids of >= this many capped waves
+#endif
 #ifndef EP_DISPATCH_TPC
 #define EP_DISPATCH_TPC 2              // tokens per CTA, bulk path (divides 32)
 #endif
@@ -205,8 +208,10 @@ __device__ __forceinline__ uint32_t quant4(const float *f, float scale) {
 // elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
 // Dev. 34(1), 1990).  For scale >= 2^-90 the residual x - q0*scale is exact
 // for every quotient large enough to give a nonzero code, and the E4M3 code
-// of the result equals that of the IEEE quotient for every bf16 x (checked
-// exhaustively over all bf16 x and block maxima); smaller scales divide.  The
+// of the result equals that of the IEEE quotient for every bf16 x under every
+// bf16 block maximum (fp8_quotient_check_kernel below compares the codes over
+// all 1.07e9 pairs; ep_test_fp8_quotient_check runs it); smaller scales
+// divide.  The
 // residual is formed negated, q0*scale - x (the same magnitude: RN is
 // symmetric), and applied with -r, so that for x = +-0 the sums of zeros
 // keep the sign of x (the code of -0 is 0x80) with no sign fix-up.
@@ -218,8 +223,9 @@ __device__ __forceinline__ float quot_recip(float x, float scale, float r) {
 
 // fl32(a / 448) for a block maximum a > 0 (a bf16 magnitude): the product
 // with RN(1/448) and the same one-FMA correction.  Equal to the IEEE
-// quotient for every finite non-negative bf16 a (checked exhaustively in
-// exact rational arithmetic); a = inf gives inf.
+// quotient for every finite non-negative bf16 a (proved on the host in exact
+// rational arithmetic, and compared on the device for every positive finite
+// a by fp8_quotient_check_kernel); a = inf gives inf.
 __device__ __forceinline__ float block_scale(float a) {
 #if EP_FP8_RECIP_QUOT
     constexpr float kInv448 = 0x1.24924ap-9f;   // RN(1/448)
@@ -243,6 +249,83 @@ __device__ __forceinline__ uint32_t quant4_recip(const float *f, float scale, fl
         packed |= (uint32_t)q << (16 * i);
     }
     return packed;
+}
+
+// ------------------------------------------- quotient check (test harness)
+// Every finite bf16 x under every positive finite bf16 block maximum a
+// (|x| <= a, both signs): the block scale above against the IEEE quotient
+// a / 448, and the codes of the dispatch's quotient (the reciprocal and one
+// correction where the scale is >= 2^-90, as in dispatch_kernel) against the
+// codes of the IEEE quotient x / scale.  One CTA per maximum; counts[0] =
+// pairs, [1] = code mismatches, [2] = scale mismatches, [3] = pairs that took
+// the reciprocal form.
+constexpr int kQuotCheckThreads = 256;
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) {
+    return __uint_as_float(b << 16);
+}
+
+__global__ void __launch_bounds__(kQuotCheckThreads)
+fp8_quotient_check_kernel(unsigned long long *counts) {
+    const uint32_t abits = blockIdx.x + 1u;          // 0x0001 .. 0x7F7F
+    const float a = bf16_bits_to_float(abits);
+    const float scale = block_scale(a);
+    const float ieee_scale = a / 448.0f;
+    const bool recip = EP_FP8_RECIP_QUOT && scale >= 0x1p-90f;
+    const float r = __frcp_rn(scale);
+    unsigned long long pairs = 0, bad = 0, fast = 0;
+    // magnitudes 0..abits, four at a time, both signs
+    for (uint32_t m0 = threadIdx.x * 4u; m0 <= abits; m0 += kQuotCheckThreads * 4u) {
+        float f[4], g[4];
+        int n = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t m = m0 + i;
+            const bool in = m <= abits;
+            n += in ? 1 : 0;
+            f[i] = in ? bf16_bits_to_float(m) : 0.0f;
+            g[i] = -f[i];
+        }
+        const uint32_t mask = n == 4 ? 0xffffffffu : ((1u << (8 * n)) - 1u);
+        const uint32_t want_p = quant4(f, ieee_scale);
+        const uint32_t want_n = quant4(g, ieee_scale);
+        const uint32_t got_p = recip ? quant4_recip(f, scale, r) : quant4(f, scale);
+        const uint32_t got_n = recip ? quant4_recip(g, scale, r) : quant4(g, scale);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t bm = 0xffu << (8 * i);
+            if (bm & mask) {
+                bad += ((want_p ^ got_p) & bm) ? 1 : 0;
+                bad += ((want_n ^ got_n) & bm) ? 1 : 0;
+            }
+        }
+        pairs += 2u * (unsigned)n;
+        fast += recip ? 2u * (unsigned)n : 0u;
+    }
+    // block totals, then one atomic per counter
+    __shared__ unsigned long long s_sum[3][kQuotCheckThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        pairs += __shfl_xor_sync(0xffffffffu, pairs, o);
+        bad += __shfl_xor_sync(0xffffffffu, bad, o);
+        fast += __shfl_xor_sync(0xffffffffu, fast, o);
+    }
+    if (lane == 0) {
+        s_sum[0][warp] = pairs;
+        s_sum[1][warp] = bad;
+        s_sum[2][warp] = fast;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long t[3] = {0, 0, 0};
+        for (int w = 0; w < kQuotCheckThreads / 32; ++w)
+            for (int i = 0; i < 3; ++i) t[i] += s_sum[i][w];
+        atomicAdd(counts + 0, t[0]);
+        atomicAdd(counts + 1, t[1]);
+        if (__float_as_uint(scale) != __float_as_uint(ieee_scale)) atomicAdd(counts + 2, 1ull);
+        atomicAdd(counts + 3, t[2]);
+    }
 }
 
 // ------------------------------------------------------------ register path
@@ -563,6 +646,7 @@ cudaError_t launch_dispatch_bulk(const Config &c, const DispatchParams &p, bool 
     static std::atomic<size_t> configured[kMaxDevices];
     static std::atomic<long> per_sm[kMaxDevices];
     static std::atomic<long> fixed[kMaxDevices];   // reserved + static shared memory per CTA
+    static std::atomic<int> sms[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -570,25 +654,33 @@ cudaError_t launch_dispatch_bulk(const Config &c, const DispatchParams &p, bool 
     const size_t row = (size_t)p.row_bytes;
     size_t dyn = (size_t)STAGES * row;
     const size_t per_cta = (size_t)TPC * (size_t)(c.W < c.k ? c.W : c.k) * row;
+    const long blocks = (long)c.G * (kChunk / TPC);
     if (EP_DISPATCH_BULK_CTAS_PER_SM > 0 && per_cta >= 64 * 1024) {
         if (per_sm[dev].load(std::memory_order_acquire) == 0) {
-            int sm_bytes = 0, reserved = 0;
+            int sm_bytes = 0, reserved = 0, n_sm = 0;
             cudaFuncAttributes fa;
             if ((e = cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
                                             dev)) != cudaSuccess ||
                 (e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock,
                                             dev)) != cudaSuccess ||
+                (e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) !=
+                    cudaSuccess ||
                 (e = cudaFuncGetAttributes(&fa, dispatch_bulk_kernel<STAGES, TPC>)) != cudaSuccess)
                 return e;
             fixed[dev].store((long)reserved + (long)fa.sharedSizeBytes, std::memory_order_relaxed);
+            sms[dev].store(n_sm, std::memory_order_relaxed);
             per_sm[dev].store(sm_bytes, std::memory_order_release);
         }
         long ctas = (long)(kBulkStreamBytes / row);
         if (ctas < EP_DISPATCH_BULK_CTAS_PER_SM) ctas = EP_DISPATCH_BULK_CTAS_PER_SM;
-        const long share = (per_sm[dev].load(std::memory_order_acquire) / ctas -
-                            fixed[dev].load(std::memory_order_relaxed)) &
-                           ~127L;
-        if (share > 0 && (size_t)share > dyn) dyn = (size_t)share;
+        // short grids keep full residency: fewer, fuller waves
+        const long capped_wave = ctas * (long)sms[dev].load(std::memory_order_relaxed);
+        if (blocks >= (long)EP_DISPATCH_BULK_CAP_MIN_WAVES * capped_wave) {
+            const long share = (per_sm[dev].load(std::memory_order_acquire) / ctas -
+                                fixed[dev].load(std::memory_order_relaxed)) &
+                               ~127L;
+            if (share > 0 && (size_t)share > dyn) dyn = (size_t)share;
+        }
     }
     if (dyn > configured[dev].load(std::memory_order_acquire)) {   // opt in to the dynamic size
         // never lower the attribute under a concurrent launch that needs more
@@ -654,6 +746,13 @@ cudaError_t launch_dispatch_recv(const Config &c, const Workspace &ws,
     dispatch_recv_kernel<<<1, threads, 0, st>>>(
         ws.dflags, ws.words, ws.group_base + (int64_t)c.Q * c.W, ws.recv_count,
         c.W, check_flags ? 1 : 0, epoch, c.timeout_ns);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_quotient_check(unsigned long long *d_counts, cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(d_counts, 0, 4 * sizeof(unsigned long long), st);
+    if (e != cudaSuccess) return e;
+    fp8_quotient_check_kernel<<<0x7F7F, kQuotCheckThreads, 0, st>>>(d_counts);
     return cudaGetLastError();
 }
 

@@ -7,6 +7,27 @@
 
 #include "../../include/ep_api.h"
 
+// NVTX ranges around every entry point, for timelines and for `ncu --nvtx`
+// range filters: compiled in with -DEP_NVTX=1 (the build's EP_NVTX=1
+// environment switch), absent otherwise, so the timed build carries none.
+#ifndef EP_NVTX
+#define EP_NVTX 0
+#endif
+#if EP_NVTX
+#include <nvtx3/nvToolsExt.h>
+namespace ep {
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+}  // namespace ep
+#define EP_RANGE(name) ::ep::NvtxRange ep_nvtx_range_(name)
+#else
+#define EP_RANGE(name) ((void)0)
+#endif
+
 namespace ep {
 
 // Tokens per layout chunk: one warp ballots over 32 tokens, so a chunk's
@@ -133,6 +154,9 @@ cudaError_t launch_moe_ungroup(const Config &c, const Workspace &ws, const char 
 cudaError_t launch_identity_expert(const Config &c, const Workspace &ws,
                                    char *y, int64_t y_stride, cudaStream_t st);
 
+// Test harness: the FP8 quotient and scale identities over every bf16 pair.
+cudaError_t launch_fp8_quotient_check(unsigned long long *d_counts, cudaStream_t st);
+
 }  // namespace ep
 
 // Host handle.
@@ -150,4 +174,5 @@ struct ep_handle {
     bool moe_valid;         // a standard-MoE grouping exists for ungroup
     ep::TokenCounts layout_nt;
     int log_level;
+    uint32_t *h_err;        // pinned host word for ep_get_error
 };

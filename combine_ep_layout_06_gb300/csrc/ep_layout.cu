@@ -65,13 +65,21 @@ layout_kernel(const LayoutParams p) {
         uint32_t mask = 0;
         bool bad = false;
         if (t < p.nt.n[s]) {
+            // all k ids are loaded before the first is used, so the lane
+            // waits for one memory latency rather than k in a row
             const int32_t *row = p.idx + ((int64_t)s * p.T + t) * p.k;
-            for (int j = 0; j < p.k; ++j) {
-                const int32_t e = __ldg(row + j);
-                if ((uint32_t)e < (uint32_t)p.E)
-                    mask |= 1u << (e / p.Er);
-                else
-                    bad = true;
+            int32_t e[EP_MAX_TOPK];
+#pragma unroll
+            for (int j = 0; j < EP_MAX_TOPK; ++j)
+                if (j < p.k) e[j] = __ldg(row + j);
+#pragma unroll
+            for (int j = 0; j < EP_MAX_TOPK; ++j) {
+                if (j < p.k) {
+                    if ((uint32_t)e[j] < (uint32_t)p.E)
+                        mask |= 1u << (e[j] / p.Er);
+                    else
+                        bad = true;
+                }
             }
         }
         if (bad) set_error(p.words, EP_DEVERR_BAD_INDEX);

@@ -49,8 +49,9 @@
  * Conventions.
  *  - Pointers named d_* are device pointers, h_* host pointers.  Streams are
  *    cudaStream_t passed as void* (NULL = the legacy default stream).
- *  - Every call is asynchronous on the given stream and allocates nothing.
- *    ep_get_error synchronises the stream it is given.
+ *  - Every call after ep_create is asynchronous on the given stream and
+ *    allocates nothing (ep_create takes one pinned host word for
+ *    ep_get_error).  ep_get_error synchronises the stream it is given.
  *  - Device-side problems (an expert id outside [0,E), a rank receiving more
  *    than cap rows, a wait that timed out, combine indices that differ from
  *    the dispatch's) set bits of a sticky device error word; the kernels skip
@@ -108,7 +109,9 @@ typedef struct {
     int32_t world_size;               /* W, 1..32 */
     int32_t num_experts;              /* E, multiple of W */
     int32_t topk;                     /* k, 1..32 */
-    int32_t hidden;                   /* H, multiple of 8 (of 128 for FP8) */
+    int32_t hidden;                   /* H, multiple of 8 (of 128 for FP8),
+                                         8..2^24 (16384 at most for the fused
+                                         FP8 dispatch) */
     int32_t max_tokens_per_rank;      /* T >= 1 */
     int32_t max_recv_tokens_per_rank; /* cap; 0 selects W*T (exact worst case) */
     int32_t dispatch_dtype;           /* EP_DT_BF16, or EP_DT_FP8_E4M3 for the
@@ -180,7 +183,8 @@ ep_status_t ep_workspace_size(const ep_config_t *cfg, size_t *bytes);
 
 /* Validate cfg, carve d_workspace (>= ep_workspace_size bytes, 256-byte
  * aligned, owned by the caller and kept alive until ep_destroy), zero the
- * flags, counters and error word (synchronously), and return a host handle.
+ * flags, counters and error word (synchronously), take one pinned host word
+ * (cudaHostAlloc) for ep_get_error, and return a host handle.
  * Reads EP_EARLY_NOTIFY / EP_FUSED_RECV / EP_LOG_LEVEL from the environment
  * once, here.  Must be called with the workspace's device current. */
 ep_status_t ep_create(const ep_config_t *cfg, void *d_workspace, size_t bytes,
@@ -216,9 +220,13 @@ ep_status_t ep_dispatch_send(ep_handle_t *h, const void *d_x, const float *d_w,
                              const int32_t *h_num_tokens, void *stream);
 
 /* Receive phase of dispatch on `stream` (may differ from the send stream):
- * wait for the send (stream-ordered via an event the send recorded), check
- * the ready flags (early_notify; bounded wait, TIMEOUT bit on expiry), then
- * write recv_count (zero included).  BAD_STATE without a pending send. */
+ * wait for the send (stream-ordered via an event the send recorded); with
+ * early_notify, check the ready flags (bounded wait, TIMEOUT bit on expiry)
+ * and then write recv_count (zero included).  Without early_notify the
+ * send's layout kernel has produced recv_count and this phase launches no
+ * kernel.  Either way the received rows and recv_count are ready on
+ * `stream` once this call's work there is done.  BAD_STATE without a
+ * pending send. */
 ep_status_t ep_dispatch_recv(ep_handle_t *h, void *stream);
 
 /* Send + receive on one stream. */
@@ -254,7 +262,10 @@ ep_status_t ep_get_combine_input_scales(const ep_handle_t *h, float **d_ptr,
                                         int64_t *rank_stride_bytes);
 
 /* Send phase of combine (expert side): records the completion of the
- * expert's work on `stream` and (early_notify) posts combine ready flags. */
+ * expert's work on `stream` and (early_notify) posts combine ready flags.
+ * BAD_STATE without a dispatch, while a dispatch send waits for its receive
+ * phase (the receive orders the expert side after the send's copy), or while
+ * an earlier combine send waits for its receive. */
 ep_status_t ep_combine_send(ep_handle_t *h, void *stream);
 
 /* Receive phase of combine (source side): wait for the combine send, then
@@ -274,7 +285,9 @@ ep_status_t ep_combine_recv(ep_handle_t *h, const void *d_y,
                             int64_t w_rank_stride_bytes, const int32_t *d_idx,
                             void *d_out, float *d_out_w, void *stream);
 
-/* Send + receive on one stream. */
+/* Send + receive on one stream.  BAD_STATE without a dispatch, while a
+ * dispatch send waits for its receive phase, or while a combine send waits
+ * for its receive. */
 ep_status_t ep_combine(ep_handle_t *h, const void *d_y,
                        int64_t y_rank_stride_bytes, const float *d_w_in,
                        int64_t w_rank_stride_bytes, const int32_t *d_idx,
@@ -320,9 +333,11 @@ ep_status_t ep_moe_ungroup(ep_handle_t *h, const void *d_yg,
  * `stream` and forget the layout (combine then needs a new dispatch). */
 ep_status_t ep_reset(ep_handle_t *h, void *stream);
 
-/* Synchronise `stream`, read and clear the device error word.  *mask gets
- * the EP_DEVERR_* bits; the return is EP_SUCCESS for 0, else the status of
- * the lowest set bit (BAD_INDEX, CAPACITY, TIMEOUT, BAD_STATE for a combine
+/* Read and clear the device error word in `stream` order, then wait for
+ * that stream alone (cudaStreamSynchronize; work on other streams keeps
+ * running, and what it sets later shows in a later call).  *mask gets the
+ * EP_DEVERR_* bits; the return is EP_SUCCESS for 0, else the status of the
+ * lowest set bit (BAD_INDEX, CAPACITY, TIMEOUT, BAD_STATE for a combine
  * mismatch). */
 ep_status_t ep_get_error(ep_handle_t *h, uint32_t *mask, void *stream);
 
@@ -338,6 +353,19 @@ ep_status_t ep_get_error(ep_handle_t *h, uint32_t *mask, void *stream);
 ep_status_t ep_test_identity_expert(ep_handle_t *h, void *d_y,
                                     int64_t y_rank_stride_bytes, void *stream);
 
+/* Test harness, not part of the hot path: checks the arithmetic behind the
+ * fused FP8 quantisation of dispatch (per 128-element block a = max|x|,
+ * scale = fl32(a/448), q = RNE-satfinite(fl32(x/scale)); OCP E4M3, "Choosing
+ * an EP API and backend", "EPv2 configuration and lifecycle") over every
+ * positive finite bf16 block maximum a and every finite bf16 x with
+ * |x| <= a, both signs (1 065 402 238 pairs), using the dispatch kernel's
+ * own device functions.  d_counts: 4 device uint64 (8-byte aligned), zeroed
+ * here, then [0] = pairs checked, [1] = pairs whose E4M3 code differs from
+ * the code of the IEEE quotient x / (a / 448), [2] = block maxima whose scale
+ * differs from the IEEE quotient a / 448, [3] = pairs that took the
+ * reciprocal-and-correction quotient.  Asynchronous on `stream`. */
+ep_status_t ep_test_fp8_quotient_check(uint64_t *d_counts, void *stream);
+
 /* Routing layout without any allocation, for callers that cannot allocate
  * device memory or pass a workspace: code living inside another
  * framework's memory pool that only sees raw tensor pointers, and serving
@@ -350,13 +378,16 @@ ep_status_t ep_test_identity_expert(ep_handle_t *h, void *d_y,
  *   d_send_counts [W][W], d_recv_count [W]; d_error: NULL or a device u32
  *   that gets EP_DEVERR_BAD_INDEX OR-ed in (out-of-range ids contribute no
  *   destination).
- * Scratch is a fixed device array inside the library (about 1.06 MB, held
+ * Scratch is a fixed device array inside the library (about 0.66 MB, held
  * by every GPU that loads the library until the process exits); it limits
- * the layout to W <= 32 and W * ceil(T/32) <= 4128 chunks (131072 tokens
- * for T a multiple of 32).  Larger sizes return EP_ERR_INVALID_ARGS.  The
- * first call on a device looks the array up (with that device current);
- * make it before any stream capture.  All calls share the array: calls
- * whose work overlaps on the GPU race; order them on one stream. */
+ * the layout to W <= 32 and W * ceil(T/32) <= 4128 32-token chunks: any
+ * W * T <= 131072 is accepted whatever T is, and up to 132096 tokens when T
+ * is a multiple of 32.  Larger sizes return EP_ERR_INVALID_ARGS.  Every call
+ * looks the array's device address up with the caller's device current (a
+ * host-side lookup once the library's device code is loaded, so a context
+ * reset in between is harmless); the first call on a device may load that
+ * code, so make it before any stream capture.  All calls share the array:
+ * calls whose work overlaps on the GPU race; order them on one stream. */
 ep_status_t ep_layout_noalloc(int32_t world_size, int32_t num_experts,
                               int32_t topk, int32_t max_tokens_per_rank,
                               const int32_t *d_idx, const int32_t *h_num_tokens,

@@ -91,6 +91,12 @@ def _declare(L):
         "or_combine_fp8": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
         "or_quant_block_f32": (None, [_P, _I, _P, _P]),
         "or_combine": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+        "or_dispatch_range": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P,
+                                   _P, _P, _P, _P, _P, _L, _L]),
+        "or_identity_expert_range": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
+                                          _P, _P, _L, _L]),
+        "or_combine_range": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
+                                  _L, _L]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -423,3 +429,61 @@ def run_all(inp, cap=None):
     out, out_w = combine(wl, inp.num_tokens, pos, y, d["out_w"], cap)
     return dict(pos=pos, C=C, recv_count=rc, cap=cap, y=y, combined=out,
                 combined_w=out_w, **d)
+
+
+# ------------------------------------------- into preallocated buffers, by range
+# The timed CPU baseline: the same C functions, run over disjoint slices of
+# independent tokens (dispatch, combine) or receive rows (identity expert) on
+# several host threads; ctypes releases the GIL for the duration of each call.
+
+def run_ranges(fn, n, threads):
+    """fn(lo, hi) over `threads` contiguous slices of [0, n), one thread each."""
+    import concurrent.futures as cf
+    threads = max(1, min(int(threads), n)) if n > 0 else 1
+    bounds = [n * i // threads for i in range(threads + 1)]
+    if threads == 1:
+        fn(0, n)
+        return
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(lambda i: fn(bounds[i], bounds[i + 1]), range(threads)))
+
+
+def dispatch_buffers(wl, cap, fp8=None):
+    """Receive buffers [W][cap][...] for dispatch_into (contents unspecified)."""
+    W, H, k = wl.world_size, wl.hidden, wl.topk
+    fp8 = wl.fp8 if fp8 is None else fp8
+    nb = H // 128 if fp8 else 0
+    return dict(out=np.empty((W, cap, H), np.uint8 if fp8 else np.uint16),
+                out_scales=np.empty((W, cap, max(nb, 1)), np.float32),
+                out_w=np.empty((W, cap, k), np.float32),
+                out_idx=np.empty((W, cap, k), np.int32),
+                src_pos=np.empty((W, cap), np.int32))
+
+
+def dispatch_into(wl, x_bits, w, idx, num_tokens, pos, cap, bufs, g0, g1, fp8=None):
+    """Dispatch of source tokens g0 <= s*T + t < g1 into preallocated buffers
+    (arrays must be C-contiguous of the dispatch_buffers types)."""
+    W, T, H, k = wl.world_size, wl.max_tokens_per_rank, wl.hidden, wl.topk
+    fp8 = wl.fp8 if fp8 is None else fp8
+    lib().or_dispatch_range(W, k, T, H, cap, int(fp8), _p(x_bits), _p(w), _p(idx),
+                            _p(num_tokens), _p(pos), _p(bufs["out"]),
+                            _p(bufs["out_scales"]), _p(bufs["out_w"]),
+                            _p(bufs["out_idx"]), _p(bufs["src_pos"]), int(g0), int(g1))
+
+
+def identity_expert_into(wl, recv_count, bufs, cap, y, i0, i1, fp8=None):
+    """Identity expert of receive rows i0 <= r*cap + p < i1 into y [W][cap][H]."""
+    W, H, k = wl.world_size, wl.hidden, wl.topk
+    fp8 = wl.fp8 if fp8 is None else fp8
+    lib().or_identity_expert_range(W, wl.num_experts, k, H, cap, int(fp8),
+                                   _p(recv_count), _p(bufs["out"]),
+                                   _p(bufs["out_scales"]), _p(bufs["out_w"]),
+                                   _p(bufs["out_idx"]), _p(y), int(i0), int(i1))
+
+
+def combine_into(wl, num_tokens, pos, y, w_in, cap, out, out_w, g0, g1):
+    """Combine of source tokens g0 <= s*T + t < g1 into out [W][T][H] (and
+    out_w [W][T][k] when w_in is given)."""
+    W, T, H, k = wl.world_size, wl.max_tokens_per_rank, wl.hidden, wl.topk
+    lib().or_combine_range(W, k, T, H, cap, _p(num_tokens), _p(pos), _p(y),
+                           _p(w_in), _p(out), _p(out_w), int(g0), int(g1))

@@ -242,47 +242,57 @@ int or_layout(int W, int E, int k, int T, const int32_t *idx,
  * Outputs are dense [W][cap][...]; rows never written are left as they are.
  * out is uint16 [W][cap][H] for bf16, uint8 [W][cap][H] for FP8; with
  * out == NULL only the per-row metadata (scales excepted) is produced. */
+/* Dispatch of the source tokens g = s*T + t with g0 <= g < g1 (t < n_s):
+ * each goes to row pos[s][t][r] of every r in D(s,t).  Tokens are
+ * independent, so disjoint ranges may run on different threads; the whole
+ * method is the range [0, W*T). */
+int or_dispatch_range(int W, int k, int T, int H, int cap, int fp8,
+                      const uint16_t *x, const float *w, const int32_t *idx,
+                      const int32_t *num_tokens, const int32_t *pos,
+                      void *out, float *out_scales, float *out_w,
+                      int32_t *out_idx, int32_t *src_pos, int64_t g0, int64_t g1)
+{
+    int nb = fp8 ? H / 128 : 0;
+    for (int64_t g = g0; g < g1; ++g) {
+        int s = (int)(g / T), t = (int)(g % T);
+        if (t >= num_tokens[s]) continue;
+        const uint16_t *row = x + ((int64_t)s * T + t) * H;
+        for (int r = 0; r < W; ++r) {
+            int32_t p = pos[((int64_t)s * T + t) * W + r];
+            if (p < 0 || p >= cap) continue;
+            int64_t rp = (int64_t)r * cap + p;
+            if (!out) {
+                /* metadata only */
+            } else if (fp8) {
+                uint8_t *o = (uint8_t *)out + rp * H;
+                for (int b = 0; b < nb; ++b)
+                    or_quant_block(row + b * 128, 128, o + b * 128,
+                                   out_scales + rp * nb + b);
+            } else {
+                uint16_t *o = (uint16_t *)out + rp * H;
+                for (int h = 0; h < H; ++h) o[h] = row[h];
+            }
+            for (int j = 0; j < k; ++j) {
+                out_w[rp * k + j] = w[((int64_t)s * T + t) * k + j];
+                out_idx[rp * k + j] = idx[((int64_t)s * T + t) * k + j];
+            }
+            src_pos[rp] = s * T + t;
+        }
+    }
+    return OR_OK;
+}
+
 int or_dispatch(int W, int k, int T, int H, int cap, int fp8,
                 const uint16_t *x, const float *w, const int32_t *idx,
                 const int32_t *num_tokens, const int32_t *pos,
                 void *out, float *out_scales, float *out_w,
                 int32_t *out_idx, int32_t *src_pos)
 {
-    int nb = fp8 ? H / 128 : 0;
-    for (int s = 0; s < W; ++s)
-        for (int t = 0; t < num_tokens[s]; ++t) {
-            const uint16_t *row = x + ((int64_t)s * T + t) * H;
-            for (int r = 0; r < W; ++r) {
-                int32_t p = pos[((int64_t)s * T + t) * W + r];
-                if (p < 0 || p >= cap) continue;
-                int64_t rp = (int64_t)r * cap + p;
-                if (!out) {
-                    /* metadata only */
-                } else if (fp8) {
-                    uint8_t *o = (uint8_t *)out + rp * H;
-                    for (int b = 0; b < nb; ++b)
-                        or_quant_block(row + b * 128, 128, o + b * 128,
-                                       out_scales + rp * nb + b);
-                } else {
-                    uint16_t *o = (uint16_t *)out + rp * H;
-                    for (int h = 0; h < H; ++h) o[h] = row[h];
-                }
-                for (int j = 0; j < k; ++j) {
-                    out_w[rp * k + j] = w[((int64_t)s * T + t) * k + j];
-                    out_idx[rp * k + j] = idx[((int64_t)s * T + t) * k + j];
-                }
-                src_pos[rp] = s * T + t;
-            }
-        }
-    return OR_OK;
+    return or_dispatch_range(W, k, T, H, cap, fp8, x, w, idx, num_tokens, pos,
+                             out, out_scales, out_w, out_idx, src_pos,
+                             0, (int64_t)W * T);
 }
 
-/* Dispatched rows of a sample of receive slots: for i < n, (r, p) =
- * (ranks[i], slots[i]) with p < min(recv_count[r], cap).  The source token
- * of the slot is the unique (s,t) with pos[s][t][r] == p, found by scanning
- * the layout; row i of the outputs is what dispatch writes to that slot
- * (payload [n][H] as uint16 or uint8, scales [n][H/128], w and idx [n][k],
- * src_pos [n]).  Returns OR_EINVAL if a slot has no source token. */
 int or_dispatch_rows(int W, int k, int T, int H, int fp8,
                      const uint16_t *x, const float *w, const int32_t *idx,
                      const int32_t *num_tokens, const int32_t *pos,
@@ -348,28 +358,37 @@ static void identity_row(int r, int Er, int k, int H, int fp8,
 
 /* Identity expert over whole receive buffers: every received row
  * p < min(recv_count[r], cap) of every rank r.  y is uint16 [W][cap][H]. */
+/* Identity expert over the receive rows i = r*cap + p with i0 <= i < i1
+ * (p < min(recv_count[r], cap)); rows are independent. */
+int or_identity_expert_range(int W, int E, int k, int H, int cap, int fp8,
+                             const int32_t *recv_count, const void *payload,
+                             const float *scales, const float *out_w,
+                             const int32_t *out_idx, uint16_t *y,
+                             int64_t i0, int64_t i1)
+{
+    int Er = E / W;
+    int nb = fp8 ? H / 128 : 0;
+    for (int64_t rp = i0; rp < i1; ++rp) {
+        int r = (int)(rp / cap), p = (int)(rp % cap);
+        int n = recv_count[r] < cap ? recv_count[r] : cap;
+        if (p >= n) continue;
+        const void *row = fp8 ? (const void *)((const uint8_t *)payload + rp * H)
+                              : (const void *)((const uint16_t *)payload + rp * H);
+        identity_row(r, Er, k, H, fp8, row, fp8 ? scales + rp * nb : 0,
+                     out_w + rp * k, out_idx + rp * k, y + rp * H);
+    }
+    return OR_OK;
+}
+
 int or_identity_expert(int W, int E, int k, int H, int cap, int fp8,
                        const int32_t *recv_count, const void *payload,
                        const float *scales, const float *out_w,
                        const int32_t *out_idx, uint16_t *y)
 {
-    int Er = E / W;
-    int nb = fp8 ? H / 128 : 0;
-    for (int r = 0; r < W; ++r) {
-        int n = recv_count[r] < cap ? recv_count[r] : cap;
-        for (int p = 0; p < n; ++p) {
-            int64_t rp = (int64_t)r * cap + p;
-            const void *row = fp8 ? (const void *)((const uint8_t *)payload + rp * H)
-                                  : (const void *)((const uint16_t *)payload + rp * H);
-            identity_row(r, Er, k, H, fp8, row, fp8 ? scales + rp * nb : 0,
-                         out_w + rp * k, out_idx + rp * k, y + rp * H);
-        }
-    }
-    return OR_OK;
+    return or_identity_expert_range(W, E, k, H, cap, fp8, recv_count, payload,
+                                    scales, out_w, out_idx, y, 0, (int64_t)W * cap);
 }
 
-/* Identity expert of n listed rows: row i was received on rank ranks[i];
- * payload [n][H] (uint16 or uint8), scales [n][H/128], w and idx [n][k]. */
 int or_identity_rows(int W, int E, int k, int H, int fp8, const int32_t *ranks,
                      int n, const void *payload, const float *scales,
                      const float *w, const int32_t *idx, uint16_t *y)
@@ -443,16 +462,28 @@ int or_combine_gathered(int nd, int H, const uint16_t *rows, uint16_t *out)
 
 /* Combine of every present token: out uint16 [W][T][H], out_w float
  * [W][T][k] (nullable with w_in).  Rows t >= n_s are left as they are. */
+/* Combine of the source tokens g = s*T + t with g0 <= g < g1 (t < n_s);
+ * tokens are independent. */
+int or_combine_range(int W, int k, int T, int H, int cap, const int32_t *num_tokens,
+                     const int32_t *pos, const uint16_t *y, const float *w_in,
+                     uint16_t *out, float *out_w, int64_t g0, int64_t g1)
+{
+    for (int64_t g = g0; g < g1; ++g) {
+        int s = (int)(g / T), t = (int)(g % T);
+        if (t >= num_tokens[s]) continue;
+        combine_token(W, k, T, H, cap, s, t, pos, y, w_in,
+                      out + ((int64_t)s * T + t) * H,
+                      out_w ? out_w + ((int64_t)s * T + t) * k : 0);
+    }
+    return OR_OK;
+}
+
 int or_combine(int W, int k, int T, int H, int cap, const int32_t *num_tokens,
                const int32_t *pos, const uint16_t *y, const float *w_in,
                uint16_t *out, float *out_w)
 {
-    for (int s = 0; s < W; ++s)
-        for (int t = 0; t < num_tokens[s]; ++t)
-            combine_token(W, k, T, H, cap, s, t, pos, y, w_in,
-                          out + ((int64_t)s * T + t) * H,
-                          out_w ? out_w + ((int64_t)s * T + t) * k : 0);
-    return OR_OK;
+    return or_combine_range(W, k, T, H, cap, num_tokens, pos, y, w_in, out, out_w,
+                            0, (int64_t)W * T);
 }
 
 /* ------------------------------------------- pre-quantised FP8 dispatch */

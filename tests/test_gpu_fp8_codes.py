@@ -100,3 +100,29 @@ def test_fused_fp8_codes_every_bf16_value_under_many_block_maxima():
         assert np.array_equal(op.out[r, :n].cpu().numpy(), q), r
         assert np.array_equal(op.out_scales[r, :n].cpu().numpy().view(np.uint32), sc.view(np.uint32))
     assert op.get_error() == (0, 0)
+
+
+def test_fp8_quotient_and_scale_identities_over_every_bf16_pair():
+    """The fused quantisation's arithmetic over every positive finite bf16
+    block maximum a and every finite bf16 x with |x| <= a, both signs: the
+    block scale equals the IEEE quotient a / 448 for every a, and the E4M3
+    code of the dispatch's quotient (reciprocal plus one correction where the
+    scale is >= 2^-90, a plain division below) equals the code of the IEEE
+    quotient x / scale for every pair.  The library runs the dispatch
+    kernel's own device functions; the cast of an IEEE quotient is itself
+    pinned to the oracle's encoder by the tests above."""
+    import ctypes
+    from combine_ep_layout_06_gb300 import _lib
+    L = _lib.load()
+    counts = torch.zeros(4, dtype=torch.int64, device="cuda")
+    st = L.ep_test_fp8_quotient_check(ctypes.c_void_p(counts.data_ptr()),
+                                      ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    pairs, code_diff, scale_diff, fast = counts.cpu().tolist()
+    n_max = 0x7F7F                               # bf16 0x0001 .. 0x7F7F
+    assert pairs == sum(2 * (a + 1) for a in range(1, n_max + 1))
+    assert scale_diff == 0
+    assert code_diff == 0
+    # most pairs take the reciprocal form (scale >= 2^-90, i.e. a >= 448 * 2^-90)
+    assert fast > pairs // 2

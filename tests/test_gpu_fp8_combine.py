@@ -85,3 +85,46 @@ def test_fp8_combine_rejects_user_rows_and_bad_hidden():
         op.combine(input=torch.zeros_like(op.combine_input))
     with pytest.raises(EpError):
         make_op(gen.Workload("h", 2, 8, 2, 16, 200), combine_dtype="fp8_e4m3")
+
+
+def test_fp8_combine_every_code_and_extreme_scales():
+    """Codes and scales written straight into the registered buffer: every
+    E4M3 code (subnormals, signed zeros, and the NaN codes in odd rows only,
+    so that even rows carry no NaN) under scales from 2^-149 to 2^126,
+    subnormal, zero and overflowing products included.  The combined output
+    equals the oracle's bit for bit; where the oracle's sum is NaN the
+    device's is NaN as well (a NaN's payload bits are not fixed)."""
+    wl = gen.Workload("codes", 4, 16, 4, 64, 512)
+    inp = gen.make_inputs(wl)
+    op = make_op(wl, combine_dtype="fp8_e4m3")
+    x, w, idx = to_device(inp)
+    op.dispatch(x, w, None, idx)
+    torch.cuda.synchronize()
+    W, cap, H = wl.world_size, op.cap, wl.hidden
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 256, size=(W, cap, H)).astype(np.uint8)
+    codes[:, :, :256] = np.arange(256, dtype=np.uint8)
+    even = codes[:, 0::2]
+    even[(even & 0x7F) == 0x7F] -= 1                  # no NaN code in even rows
+    codes[:, 0::2] = even
+    nb = H // 128
+    exps = rng.integers(-149, 127, size=(W, cap, nb))
+    scales = np.ldexp(rng.uniform(1.0, 2.0, size=(W, cap, nb)), exps).astype(np.float32)
+    special = np.array([0.0, 2.0 ** -149, 2.0 ** -126, np.nextafter(np.float32(256), 0),
+                        256.0, 2.0 ** 126], np.float32)
+    scales[:, :special.size, 0] = special
+    scales[:, :, 1] = np.ldexp(np.float32(1.5), rng.integers(-20, 12, size=(W, cap)))
+    op.combine_input.copy_(torch.from_numpy(codes))
+    op.combine_input_scales.copy_(torch.from_numpy(scales))
+    out, out_w = op.combine(weights=op.out_w, indices=idx)
+    torch.cuda.synchronize()
+    pos, C, rc = oracle.layout(wl, inp.indices, inp.num_tokens)
+    exp, exp_w = oracle.combine_fp8(wl, inp.num_tokens, pos, codes, scales,
+                                    op.out_w.cpu().numpy(), cap)
+    got = bits(out)
+    isnan = lambda b: ((b & 0x7F80) == 0x7F80) & ((b & 0x007F) != 0)   # noqa: E731
+    assert np.array_equal(isnan(got), isnan(exp))
+    ok = ~isnan(exp)
+    assert np.array_equal(got[ok], exp[ok])
+    assert isnan(exp).any() and ok.any()
+    assert op.get_error() == (0, 0)

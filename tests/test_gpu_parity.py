@@ -315,56 +315,61 @@ def test_captured_graph_replayed_on_new_routing(name, fp8):
 
 # --------------------------------------------------------------- full size
 
-def _sample_check_full(wl, seed=0, n_rows=48, n_tok=24):
-    inp = gen.make_inputs(wl)
-    op = make_op(wl)
-    res = run_gpu(op, inp, payload=False)
-    pos, C, rc = oracle.layout(wl, inp.indices, inp.num_tokens)
-    assert np.array_equal(res["recv_count"], rc)
-    assert np.array_equal(res["send_counts"], C)
-    assert np.array_equal(res["pos"], pos)
-    meta = oracle.dispatch(wl, inp.x_bits, inp.weights, inp.indices,
-                           inp.num_tokens, pos, op.cap, payload=False)
+def _compare_per_rank(wl, inp, op, res, ref):
+    """Every received row and every combined token of a large case, rank by
+    rank (the device rows are fetched one rank at a time)."""
+    assert np.array_equal(res["recv_count"], ref["recv_count"])
+    assert np.array_equal(res["send_counts"], ref["C"])
+    assert np.array_equal(res["pos"], ref["pos"])
     for r in range(wl.world_size):
-        n = rc[r]
-        assert np.array_equal(res["src_pos"][r, :n], meta["src_pos"][r, :n])
-        assert np.array_equal(res["out_idx"][r, :n], meta["out_idx"][r, :n])
+        n = int(ref["recv_count"][r])
+        assert np.array_equal(res["src_pos"][r, :n], ref["src_pos"][r, :n]), r
+        assert np.array_equal(res["out_idx"][r, :n], ref["out_idx"][r, :n]), r
         assert np.array_equal(res["out_w"][r, :n].view(np.uint32),
-                              meta["out_w"][r, :n].view(np.uint32))
-    rng = np.random.default_rng(seed)
-    ranks = np.flatnonzero(rc > 0)
-    rr = rng.choice(ranks, size=n_rows)
-    pp = np.array([rng.integers(0, rc[r]) for r in rr])
-    pp[:len(ranks)] = rc[ranks[:n_rows]] - 1          # last row of each rank
-    rr[:len(ranks)] = ranks[:n_rows]
-    d = oracle.dispatch_rows(wl, inp.x_bits, inp.weights, inp.indices,
-                             inp.num_tokens, pos, rr, pp)
-    ri = torch.from_numpy(rr.astype(np.int64)).cuda()
-    pi = torch.from_numpy(pp.astype(np.int64)).cuda()
-    assert np.array_equal(bits(op.out[ri, pi]), d["out"])
-    if wl.fp8:
-        assert np.array_equal(bits(op.out_scales[ri, pi]),
-                              d["out_scales"].view(np.uint32))
-    y = oracle.identity_rows(wl, rr, d["out"], d["out_scales"], d["out_w"],
-                             d["out_idx"])
-    assert np.array_equal(bits(op.combine_input[ri, pi]), y)
-    T = wl.max_tokens_per_rank
-    for g in list(rng.choice(wl.world_size * T, size=n_tok)) + [0, wl.world_size * T - 1]:
-        s, t = divmod(int(g), T)
-        dest = [r for r in range(wl.world_size) if pos[s, t, r] >= 0]
-        slots = [pos[s, t, r] for r in dest]
-        dr = oracle.dispatch_rows(wl, inp.x_bits, inp.weights, inp.indices,
-                                  inp.num_tokens, pos, dest, slots)
-        yr = oracle.identity_rows(wl, dest, dr["out"], dr["out_scales"],
-                                  dr["out_w"], dr["out_idx"])
-        exp = oracle.combine_gathered(yr)
-        assert np.array_equal(res["combined"][s, t], exp), (s, t)
-    return op, res
+                              ref["out_w"][r, :n].view(np.uint32)), r
+        assert np.array_equal(bits(op.out[r, :n]), ref["out"][r, :n]), r
+        if wl.fp8:
+            assert np.array_equal(bits(op.out_scales[r, :n]),
+                                  ref["out_scales"][r, :n].view(np.uint32)), r
+        assert np.array_equal(bits(op.combine_input[r, :n]), ref["y"][r, :n]), r
+    for s in range(wl.world_size):
+        n = int(inp.num_tokens[s])
+        assert np.array_equal(res["combined"][s, :n], ref["combined"][s, :n]), s
+        assert np.array_equal(res["combined_w"][s, :n].view(np.uint32),
+                              ref["combined_w"][s, :n].view(np.uint32)), s
 
 
 @pytest.mark.parametrize("name", ["dsv3", "dsv3_fp8_zipf", "mixtral"])
-def test_parity_full_size_sampled(name):
-    _sample_check_full(gen.WORKLOADS[name])
+def test_parity_full_size_every_token(name):
+    """The benchmark's workloads at full size, in the launch configuration the
+    benchmark times (one-call dispatch, then the gather above 4096 tokens),
+    compared with the oracle on everything: layout, every received row with
+    its metadata, every identity-expert row and every combined token."""
+    wl = gen.WORKLOADS[name]
+    inp = gen.make_inputs(wl)
+    rc = oracle.layout(wl, inp.indices, inp.num_tokens)[2]
+    ref = oracle.run_all(inp, cap=int(rc.max()))   # rows past the counts stay out
+    op = make_op(wl)
+    res = run_gpu(op, inp, payload=False)
+    _compare_per_rank(wl, inp, op, res, ref)
+    assert op.get_error() == (0, 0)
+
+
+@pytest.mark.parametrize("ragged", [False, True])
+@pytest.mark.parametrize("name", ["dsv3", "dsv3_fp8_zipf", "mixtral", "ll_decode"])
+def test_parity_above_the_few_token_switch(name, ragged):
+    """More than 4096 tokens (the combine's switch between its few-token and
+    bandwidth forms) at a reduced hidden size, compared element by element."""
+    wl = gen.WORKLOADS[name]
+    wl = wl.scaled(640 if wl.world_size == 8 else 320, hidden=1024)
+    nt = gen.ragged_num_tokens(wl) if ragged else None
+    if ragged:                     # keep more than 4096 present tokens
+        nt = np.maximum(nt, wl.max_tokens_per_rank - 40)
+        nt[-1] = 0
+    inp = gen.make_inputs(wl, num_tokens=nt)
+    assert int(inp.num_tokens.sum()) > 4096
+    op = make_op(wl)
+    _compare(wl, inp, run_gpu(op, inp), op.cap)
 
 
 def test_capacity_overflow_is_bounded_and_reported():
@@ -453,7 +458,40 @@ def test_out_of_order_calls_return_bad_state():
     with pytest.raises(EpError) as e:
         op.dispatch_send(x, w, None, idx)            # send twice
     assert e.value.status == 6
+    # combine while the send waits for its receive phase
+    with pytest.raises(EpError) as e:
+        op.combine()
+    assert e.value.status == 6
+    with pytest.raises(EpError) as e:
+        op.combine_send()
+    assert e.value.status == 6
     op.dispatch_recv()
+    op.combine_send()
+    with pytest.raises(EpError) as e:
+        op.combine_send()                            # combine send twice
+    assert e.value.status == 6
+    op.combine_recv()
+    assert op.get_error() == (0, 0)
+
+
+def test_get_error_waits_for_its_own_stream_only():
+    """ep_get_error reads the error word in its stream's order and waits for
+    that stream alone: a long kernel on another stream is still running when
+    it returns."""
+    wl = gen.WORKLOADS["tiny"]
+    op = make_op(wl)
+    inp = gen.make_inputs(wl)
+    x, w, idx = to_device(inp)
+    a, b = torch.cuda.Stream(), torch.cuda.Stream()
+    op.dispatch(x, w, None, idx, stream=a)
+    done_b = torch.cuda.Event()
+    with torch.cuda.stream(b):
+        torch.cuda._sleep(2_000_000_000)             # about a second of spinning
+        done_b.record(b)
+    assert op.get_error(a) == (0, 0)
+    assert not done_b.query()                        # b was not waited for
+    torch.cuda.synchronize()
+    assert done_b.query()
 
 
 def test_host_argument_checks():

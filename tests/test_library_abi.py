@@ -75,7 +75,8 @@ def test_workspace_size_and_config_validation(L):
            dict(max_tokens_per_rank=0), dict(dispatch_dtype=1, hidden=7168 + 8),
            dict(dispatch_dtype=7), dict(max_recv_tokens_per_rank=-1),
            dict(fused_recv=1, early_notify=0), dict(combine_dtype=1, hidden=7176),
-           dict(combine_dtype=5)]
+           dict(combine_dtype=5), dict(hidden=(1 << 24) + 8),
+           dict(hidden=1 << 25), dict(dispatch_dtype=1, hidden=16384 + 128)]
     for b in bad:
         assert _size(L, **b)[0] == 3, b      # EP_ERR_INVALID_ARGS
     assert _size(L, max_recv_tokens_per_rank=100)[1] < n
@@ -90,3 +91,24 @@ def test_create_rejects_bad_workspace_without_touching_the_gpu(L):
     assert L.ep_create(ctypes.byref(c), ctypes.c_void_p(0x1001), 1 << 40,
                        ctypes.byref(h)) == 3          # not 256-byte aligned
     assert L.ep_destroy(None) == 3
+
+
+def test_hidden_size_upper_bound(L):
+    """H up to 2^24 is accepted (a row's byte count stays in an int), above
+    it the config is rejected."""
+    st, n = _size(L, hidden=1 << 24, max_tokens_per_rank=1, world_size=1,
+                  num_experts=1, topk=1)
+    assert st == 0 and n >= (1 << 24) * 2 * 2
+    assert _size(L, hidden=(1 << 24) + 8, max_tokens_per_rank=1, world_size=1,
+                 num_experts=1, topk=1)[0] == 3
+
+
+def test_nvtx_build_switch_compiles(tmp_path):
+    """The entry points' NVTX ranges (compiled in with -DEP_NVTX=1, off in
+    the default build) compile for sm_103a."""
+    import subprocess
+    src = os.path.join(ROOT, "combine_ep_layout_06_gb300", "csrc", "ep_api.cu")
+    cmd = [build._nvcc(), *build.NVCC_FLAGS, "-DEP_NVTX=1", "-c", src,
+           "-o", str(tmp_path / "ep_api_nvtx.o")]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr

@@ -707,3 +707,37 @@ def test_input_recipe_properties_at_full_size():
         x = (inp.x_bits[0, :512].astype(np.uint32) << 16).view(np.float32)
         sigma = np.sqrt(2.0) if name == "mixtral" else 1.0
         assert abs(x.std() / sigma - 1) < 0.01, (name, x.std())
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_threaded_range_form_equals_whole_buffer_form(fp8):
+    """The timed CPU baseline runs the oracle's dispatch, identity expert and
+    combine over disjoint token / row ranges on several threads; the result
+    is bit-identical to the single whole-buffer calls (the pinned form)."""
+    wl = gen.Workload("thr", 4, 16, 3, 97, 256, fp8=fp8)
+    inp = gen.make_inputs(wl, num_tokens=[97, 40, 0, 61])
+    ref = oracle.run_all(inp)
+    cap = ref["cap"]
+    W, T, H, k = wl.world_size, wl.max_tokens_per_rank, wl.hidden, wl.topk
+    pos, C, rc = oracle.layout(wl, inp.indices, inp.num_tokens)
+    bufs = oracle.dispatch_buffers(wl, cap)
+    for v in bufs.values():
+        v.fill(0)
+    nt = np.ascontiguousarray(inp.num_tokens, np.int32)
+    oracle.run_ranges(lambda a, b: oracle.dispatch_into(
+        wl, inp.x_bits, inp.weights, inp.indices, nt, pos, cap, bufs, a, b), W * T, 5)
+    y = np.zeros((W, cap, H), np.uint16)
+    oracle.run_ranges(lambda a, b: oracle.identity_expert_into(
+        wl, rc, bufs, cap, y, a, b), W * cap, 7)
+    out = np.zeros((W, T, H), np.uint16)
+    out_w = np.zeros((W, T, k), np.float32)
+    oracle.run_ranges(lambda a, b: oracle.combine_into(
+        wl, nt, pos, y, bufs["out_w"], cap, out, out_w, a, b), W * T, 3)
+    for key in ("out", "out_w", "out_idx", "src_pos"):
+        assert np.array_equal(bufs[key], ref[key]), key
+    if fp8:
+        assert np.array_equal(bufs["out_scales"].view(np.uint32),
+                              ref["out_scales"].view(np.uint32))
+    assert np.array_equal(y, ref["y"])
+    assert np.array_equal(out, ref["combined"])
+    assert np.array_equal(out_w.view(np.uint32), ref["combined_w"].view(np.uint32))

@@ -68,6 +68,43 @@ def test_layout_noalloc_matches_existing_entry_point_twice():
         assert err == 0
 
 
+def test_layout_noalloc_at_its_scratch_limit():
+    """W = 32 ranks and T = 4128 tokens: exactly the 4128 chunks the scratch
+    holds, so the scan covers the whole array; twice in a row, against the
+    existing entry point."""
+    L = _lib.load()
+    wl = gen.Workload("limit", 32, 64, 2, 4128, 8)
+    for nt in (None, gen.ragged_num_tokens(wl)):
+        inp = gen.make_inputs(wl, num_tokens=nt)
+        idx = torch.from_numpy(inp.indices).cuda()
+        st, pos, sc, rc, err = _noalloc(L, wl, idx, inp.num_tokens)
+        assert st == 0 and err == 0
+        ref_pos, ref_sc, ref_rc = _existing(wl, inp)
+        assert np.array_equal(rc, ref_rc)
+        assert np.array_equal(sc, ref_sc)
+        assert np.array_equal(pos, ref_pos)
+
+
+def test_layout_noalloc_reports_out_of_range_ids():
+    """Expert ids outside [0, E) set the error bit and add no destination,
+    as in the existing entry point."""
+    L = _lib.load()
+    wl = gen.WORKLOADS["dsv3"].scaled(300, hidden=8)
+    inp = gen.make_inputs(wl)
+    inp.indices[0, 5, 1] = wl.num_experts + 3
+    inp.indices[3, 299, 0] = -1
+    inp.indices[7, 0, :] = 1 << 30                 # a token with no valid id
+    idx = torch.from_numpy(inp.indices).cuda()
+    st, pos, sc, rc, err = _noalloc(L, wl, idx, inp.num_tokens)
+    assert st == 0
+    assert err & _lib.EP_DEVERR_BAD_INDEX
+    assert np.all(pos[7, 0] == -1)
+    ref_pos, ref_sc, ref_rc = _existing(wl, inp)
+    assert np.array_equal(rc, ref_rc)
+    assert np.array_equal(sc, ref_sc)
+    assert np.array_equal(pos, ref_pos)
+
+
 def test_layout_noalloc_rejects_sizes_beyond_its_scratch():
     L = _lib.load()
     W, T = 32, 4200                       # 32 * ceil(4200/32) = 4224 chunks
