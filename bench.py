@@ -567,7 +567,7 @@ def run_ours(args, rank, world, local_rank):
         headline_entry = workload_entry_from(case, ms_per_step, (lay_ms, d_ms, c_ms), roof,
                                              peak, cpu, oracle_parity, graph is not None,
                                              args.steps)
-        if wl.name in COLD_L2 and graph is not None:
+        if wl.name in COLD_L2 and graph is not None and not args.no_workloads:
             add_cold_l2(headline_entry, case, graph, args.workload_steps)
         headline_entry["device_errors"] = int(mask)
     case.close()

@@ -47,7 +47,7 @@ namespace {
 #define EP_COMBINE_FP8_UNROLL8 1      // 16-code vectors in flight per row, <= 8 rows
 #endif
 #ifndef EP_COMBINE_FP8_PAIRS
-#define EP_COMBINE_FP8_PAIRS 0        // FP8 rows: 0 scalar, 1 two-wide adds, 2 two-wide products too
+#define EP_COMBINE_FP8_PAIRS 1        // FP8 rows: two-wide adds of scalar products (0: scalar adds)
 #endif
 
 constexpr int kCombineWarps = EP_COMBINE_WARPS;
@@ -111,19 +111,12 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
     return __half22float2(__half2(h));
 }
 
-// Two-wide fp32 multiply: each half is the IEEE round-to-nearest product.
-__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-
 // acc += fl32(value(q) * scale) for 16 codes (a rounded multiply, then a
-// rounded add); acc[i] holds elements 2i, 2i+1.
+// rounded add); acc[i] holds elements 2i, 2i+1.  The products are scalar
+// round-to-nearest multiplies; their sums into the accumulators go two at a
+// time (add.rn.f32x2, each half the scalar round-to-nearest add), which
+// measured 298 against 302 us on the DeepSeek-V3 shape.  Two-wide products
+// feeding two-wide adds came out fused (one rounding) and are not used.
 __device__ __forceinline__ void add_fp8x16(float2 acc[8], const uint4 &q, float scale) {
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -135,15 +128,11 @@ __device__ __forceinline__ void add_fp8x16(float2 acc[8], const uint4 &q, float 
         acc[2 * i].y = __fadd_rn(acc[2 * i].y, __fmul_rn(lo.y, scale));
         acc[2 * i + 1].x = __fadd_rn(acc[2 * i + 1].x, __fmul_rn(hi.x, scale));
         acc[2 * i + 1].y = __fadd_rn(acc[2 * i + 1].y, __fmul_rn(hi.y, scale));
-#elif EP_COMBINE_FP8_PAIRS == 1
+#else
         acc[2 * i] = add2_rn(acc[2 * i], make_float2(__fmul_rn(lo.x, scale),
                                                      __fmul_rn(lo.y, scale)));
         acc[2 * i + 1] = add2_rn(acc[2 * i + 1], make_float2(__fmul_rn(hi.x, scale),
                                                              __fmul_rn(hi.y, scale)));
-#else
-        const float2 s2 = make_float2(scale, scale);
-        acc[2 * i] = add2_rn(acc[2 * i], mul2_rn(lo, s2));
-        acc[2 * i + 1] = add2_rn(acc[2 * i + 1], mul2_rn(hi, s2));
 #endif
     }
 }
@@ -207,10 +196,13 @@ __device__ __forceinline__ void add_vec(float acc[8], const RowVec &r) {
 // FEW: few tokens (the gather is latency-bound): loads not allocated in L1,
 // and registers for 2 CTAs per SM rather than 3, so that no row buffer
 // spills (4096 tokens of 8 rows at most: 80 -> 70 us; decode unchanged).
+// FP8 rows take it too, with twice the column vectors in flight per row
+// (decode: 38.4 against 41.0 us; at full size the 3-CTA form stays faster,
+// 298 against 320 us on the DeepSeek-V3 shape).
 template <int MAXD, int U, bool COHERENT, int YK, bool STAGED, bool FEW = false>
 __global__ void __launch_bounds__(kCombineThreads,
-                                  YK == kYFp8 ? EP_COMBINE_FP8_MIN_BLOCKS
-                                              : (FEW ? EP_COMBINE_FEW_MIN_BLOCKS
+                                  FEW ? EP_COMBINE_FEW_MIN_BLOCKS
+                                      : (YK == kYFp8 ? EP_COMBINE_FP8_MIN_BLOCKS
                                                      : EP_COMBINE_MIN_BLOCKS))
 combine_kernel(const CombineParams p) {
     // bytes of one column vector of an expert row: bf16 16, fp32 32, FP8 8
@@ -274,13 +266,15 @@ combine_kernel(const CombineParams p) {
 #pragma unroll
             for (int j = 0; j < MAXD; ++j) {
                 if (j < nd) {
+                    const char *rj = rows[j];
+                    const char *sj = srows[j];
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
                         const int v = v0 + 32 * u;
                         if (v < nv) {
-                            q[u][j] = COHERENT ? ld_coherent16(rows[j] + (int64_t)v * 16)
-                                               : ld_stream16(rows[j] + (int64_t)v * 16);
-                            sc[u][j] = reinterpret_cast<const float *>(srows[j])[v >> 3];
+                            q[u][j] = COHERENT ? ld_coherent16(rj + (int64_t)v * 16)
+                                               : ld_stream16(rj + (int64_t)v * 16);
+                            sc[u][j] = reinterpret_cast<const float *>(sj)[v >> 3];
                         }
                     }
                 }
@@ -523,6 +517,11 @@ cudaError_t launch_combine_t(const Config &c, const CombineParams &p,
                              cudaStream_t st) {
     const int64_t tokens = (int64_t)c.W * c.T;
     const int blocks = (int)((tokens + kCombineWarps - 1) / kCombineWarps);
+    if constexpr (YK == kYFp8 && MAXD == 8) {
+        if (!COH && tokens <= kFewTokens)
+            return launch_after_previous(combine_kernel<MAXD, 2 * U, COH, YK, false, true>, blocks,
+                                         kCombineThreads, 0, st, p);
+    }
     if constexpr (YK == kYBf16) {
         if (p.stage)
             return launch_after_previous(combine_kernel<MAXD, U, COH, YK, true>, blocks,

@@ -65,10 +65,11 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p,
 
 // Two-wide fp32 add: each half is the IEEE round-to-nearest scalar add
 // (subnormals kept), one instruction for the pair on this SM generation.
-// Only for sums of values that no multiply produced: measured on sm_103a
-// with CUDA 13.0, a two-wide round-to-nearest multiply feeding a two-wide
-// add could come out fused (one rounding), even with contraction disabled,
-// so products that must be rounded on their own stay scalar.
+// Measured on sm_103a with CUDA 13.0, a two-wide round-to-nearest multiply
+// feeding a two-wide add could come out fused (one rounding), even with
+// contraction disabled, so products that must be rounded on their own are
+// scalar round-to-nearest multiplies; sums of those (the FP8 combine) and
+// of plain values use this add, and the parity tests compare every bit.
 __device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
     float2 d;
     asm("{\n\t.reg .b64 ra, rb, rd;\n\t"

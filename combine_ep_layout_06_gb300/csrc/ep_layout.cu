@@ -16,6 +16,10 @@
 namespace ep {
 namespace {
 
+#ifndef EP_LAYOUT_CLUSTER
+#define EP_LAYOUT_CLUSTER 1     // up to 8 groups: one thread-block cluster, no grid-wide ticket
+#endif
+
 constexpr int kLayoutThreads = kGroup * 32;     // one warp per chunk
 constexpr int kLayoutWarps = kGroup;
 constexpr int kScanBatch = 8;                   // group totals in registers per lane
@@ -189,6 +193,129 @@ layout_kernel(const LayoutParams p) {
     if (threadIdx.x == 0) p.words[kWordLayoutDone] = 0;   // for the next call
 }
 
+// ------------------------------------------------------- one-cluster form
+// Up to kClusterGroups groups (W * T up to ~2048 tokens, the decode sizes):
+// the Q CTAs run as ONE thread-block cluster, so the group prefix needs no
+// grid-wide ticket and no round trip through L2.  Each CTA keeps its group
+// totals in shared memory; after a cluster barrier every CTA reads the
+// totals of the CTAs before it through distributed shared memory (mapa +
+// ld.shared::cluster) for its group base, and the CTA owning the first chunk
+// of a source stores that chunk's start into CTA 0's shared memory; after a
+// second barrier CTA 0 writes the send counts.  Every thread reaches both
+// barriers, so no CTA leaves while a peer may still read its shared memory.
+// On the decode workload (8 groups) the step measured 82.5 against 84.9 us
+// with the ticket form (chained layouts alone: 5.8 against 6.3 us).
+constexpr int kClusterGroups = 8;      // the portable cluster size
+
+__device__ __forceinline__ uint32_t cluster_map(const void *local, uint32_t cta) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(cta));
+    return r;
+}
+__device__ __forceinline__ int ld_cluster(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_cluster(uint32_t addr, int v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kLayoutThreads)
+layout_cluster_kernel(const LayoutParams p) {
+    __shared__ int s_cnt[kLayoutWarps][EP_MAX_WORLD];
+    __shared__ int s_tot[EP_MAX_WORLD];                    // this group's totals
+    __shared__ int s_start[EP_MAX_WORLD + 1][EP_MAX_WORLD]; // CTA 0: first-chunk starts
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int q = blockIdx.x;                              // = rank in the cluster
+    const int g = q * kGroup + warp;
+    grid_dependency_wait();
+    grid_dependents_may_launch();
+
+    // ---- per chunk: masks and destination counts (as layout_kernel)
+    int my_count = 0;
+    if (g < p.G) {
+        const int s = g / p.nch;
+        const int t = (g - s * p.nch) * kChunk + lane;
+        uint32_t mask = 0;
+        bool bad = false;
+        if (t < p.nt.n[s]) {
+            const int32_t *row = p.idx + ((int64_t)s * p.T + t) * p.k;
+            int32_t e[EP_MAX_TOPK];
+#pragma unroll
+            for (int j = 0; j < EP_MAX_TOPK; ++j)
+                if (j < p.k) e[j] = __ldg(row + j);
+#pragma unroll
+            for (int j = 0; j < EP_MAX_TOPK; ++j) {
+                if (j < p.k) {
+                    if ((uint32_t)e[j] < (uint32_t)p.E)
+                        mask |= 1u << (e[j] / p.Er);
+                    else
+                        bad = true;
+                }
+            }
+        }
+        if (bad) set_error(p.words, EP_DEVERR_BAD_INDEX);
+        if (t < p.T) p.masks[(int64_t)s * p.T + t] = mask;
+        for (int r = 0; r < p.W; ++r) {
+            const uint32_t b = __ballot_sync(0xffffffffu, (mask >> r) & 1u);
+            if (lane == r) my_count = __popc(b);
+        }
+    }
+    s_cnt[warp][lane] = my_count;
+    __syncthreads();
+    // chunk offsets inside the group (kept in s_cnt as exclusive prefixes)
+    if (warp == 0 && lane < p.W) {
+        int run = 0;
+        for (int w = 0; w < kLayoutWarps; ++w) {
+            const int c = s_cnt[w][lane];
+            s_cnt[w][lane] = run;
+            const int gg = q * kGroup + w;
+            if (gg < p.G) p.chunk_local[(int64_t)gg * p.W + lane] = run;
+            run += c;
+        }
+        s_tot[lane] = run;
+    }
+    cluster_sync_all();                                     // every s_tot is final
+
+    // ---- group base from the totals of the CTAs before this one
+    if (warp == 0 && lane < p.W) {
+        int base = 0, total = 0;
+        for (int c = 0; c < (int)gridDim.x; ++c) {
+            const int v = ld_cluster(cluster_map(&s_tot[lane], (uint32_t)c));
+            if (c < q) base += v;
+            total += v;
+        }
+        p.group_base[(int64_t)q * p.W + lane] = base;
+        // the first chunk of every source in this group: its start, to CTA 0
+        for (int w = 0; w < kLayoutWarps; ++w) {
+            const int gg = q * kGroup + w;
+            if (gg < p.G && gg % p.nch == 0)
+                st_cluster(cluster_map(&s_start[gg / p.nch][lane], 0u), base + s_cnt[w][lane]);
+        }
+        if (q == 0) {
+            s_start[p.W][lane] = total;
+            p.group_base[(int64_t)p.Q * p.W + lane] = total;
+            if (total > p.cap) set_error(p.words, EP_DEVERR_CAPACITY);
+            if (p.publish) p.recv_count[lane] = total;
+        }
+    }
+    cluster_sync_all();                                     // every start is in CTA 0
+
+    // ---- C[s][r] = start of the first chunk of s+1 minus that of s
+    if (q == 0) {
+        for (int i = threadIdx.x; i < p.W * p.W; i += kLayoutThreads) {
+            const int s = i / p.W, r = i - s * p.W;
+            p.send_counts[i] = s_start[s + 1][r] - s_start[s][r];
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_layout(const Config &c, const Workspace &ws,
@@ -207,6 +334,25 @@ cudaError_t launch_layout(const Config &c, const Workspace &ws,
     p.nch = c.nch; p.G = c.G; p.Q = c.Q; p.cap = c.cap;
     p.publish = publish ? 1 : 0;
     p.nt = nt;
+#if EP_LAYOUT_CLUSTER
+    if (c.Q <= kClusterGroups) {
+        // one cluster of Q CTAs, launched programmatically after the kernel before it
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)c.Q);
+        cfg.blockDim = dim3(kLayoutThreads);
+        cfg.stream = st;
+        cudaLaunchAttribute at[2];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = (unsigned)c.Q;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 2;
+        return cudaLaunchKernelEx(&cfg, layout_cluster_kernel, p);
+    }
+#endif
     return launch_after_previous(layout_kernel, (unsigned)c.Q, (unsigned)kLayoutThreads, 0, st, p);
 }
 

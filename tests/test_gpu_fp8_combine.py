@@ -15,7 +15,8 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("name,T,H,ragged", [
     ("dsv3", 150, 1024, False), ("dsv3", 150, 7168, True), ("dsv3_fp8_zipf", 120, 1024, True),
-    ("mixtral", 200, 512, False), ("ll_decode", 128, 384, True), ("tiny", 128, 256, True)])
+    ("mixtral", 200, 512, False), ("ll_decode", 128, 384, True), ("tiny", 128, 256, True),
+    ("dsv3", 640, 1024, False), ("mixtral", 640, 512, True)])   # > 4096 tokens: the 3-CTA form
 def test_fp8_combine_payload_parity(name, T, H, ragged):
     wl = gen.WORKLOADS[name].scaled(T, hidden=H)
     inp = gen.make_inputs(wl, num_tokens=gen.ragged_num_tokens(wl) if ragged else None)
