@@ -327,10 +327,16 @@ __global__ void __launch_bounds__(kGroupWarps * 32) moe_group_bulk_kernel(const 
     }
 }
 
+#ifndef EP_UNGROUP_PAIRS
+#define EP_UNGROUP_PAIRS 1   // scalar products summed two at a time (952 -> 940 us, DeepSeek-V3 shape)
+#endif
+
 // Weighted fp32 sum of NE grouped rows (NE > 0 known: a fixed number of
 // entries, U column vectors per lane per pass) or of up to NE rows (the
 // general case, `ne` at run time).  Entries are taken in ascending top-k
-// slot j; the sum starts from +0 and each term is fl(w_j * y) (no FMA).
+// slot j; the sum starts from +0 and each term is fl(w_j * y) (no FMA): a
+// scalar round-to-nearest product, added with add.rn.f32x2 (each half the
+// scalar round-to-nearest add).
 template <int NE, int U, bool EXACT>
 __device__ __forceinline__ void ungroup_row(uint32_t em, int q, float w, const char *ybase,
                                             uint4 *out, int nvec, int lane) {
@@ -372,10 +378,20 @@ __device__ __forceinline__ void ungroup_row(uint32_t em, int q, float w, const c
                     const uint32_t wd[4] = {val[u][i].x, val[u][i].y, val[u][i].z, val[u][i].w};
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
+#if EP_UNGROUP_PAIRS
+                        // scalar round-to-nearest products, summed two at a time
+                        const float2 r = add2_rn(
+                            make_float2(acc[2 * h], acc[2 * h + 1]),
+                            make_float2(__fmul_rn(ws[i], __uint_as_float(wd[h] << 16)),
+                                        __fmul_rn(ws[i], __uint_as_float(wd[h] & 0xffff0000u))));
+                        acc[2 * h] = r.x;
+                        acc[2 * h + 1] = r.y;
+#else
                         acc[2 * h] = __fadd_rn(acc[2 * h],
                                                __fmul_rn(ws[i], __uint_as_float(wd[h] << 16)));
                         acc[2 * h + 1] = __fadd_rn(
                             acc[2 * h + 1], __fmul_rn(ws[i], __uint_as_float(wd[h] & 0xffff0000u)));
+#endif
                     }
                 }
             }
