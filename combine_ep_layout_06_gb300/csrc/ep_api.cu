@@ -615,14 +615,15 @@ ep_status_t ep_get_error(ep_handle_t *h, uint32_t *mask, void *stream) {
     EP_RANGE("ep_get_error");
     if (!h || !mask) return EP_ERR_INVALID_ARGS;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // Stream-ordered read and clear of the word, then a wait for this stream
-    // alone (work on other streams keeps running).  The read lands in the
-    // handle's pinned host word.
-    ep_status_t s = gpu(h, cudaMemcpyAsync(h->h_err, h->ws.words + kWordErr, 4,
-                                           cudaMemcpyDeviceToHost, st),
-                        "cudaMemcpyAsync");
+    // Stream-ordered: one atomic exchange takes the word and clears it, the
+    // taken value is copied to the handle's pinned host word, and only this
+    // stream is waited for (work on other streams keeps running; a bit it
+    // sets later is reported by a later call).
+    ep_status_t s = gpu(h, launch_take_error(h->ws, st), "take_error");
     if (s != EP_SUCCESS) return s;
-    s = gpu(h, cudaMemsetAsync(h->ws.words + kWordErr, 0, 4, st), "cudaMemsetAsync");
+    s = gpu(h, cudaMemcpyAsync(h->h_err, h->ws.words + kWordErrTaken, 4,
+                               cudaMemcpyDeviceToHost, st),
+            "cudaMemcpyAsync");
     if (s != EP_SUCCESS) return s;
     s = gpu(h, cudaStreamSynchronize(st), "cudaStreamSynchronize");
     if (s != EP_SUCCESS) return s;

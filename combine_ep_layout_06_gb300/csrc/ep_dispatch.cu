@@ -585,6 +585,10 @@ dispatch_bulk_kernel(const DispatchParams p) {
     if (p.notify) notify_source_done<TPC>(p, s);
 }
 
+__global__ void take_error_kernel(uint32_t *words) {
+    words[kWordErrTaken] = atomicExch(words + kWordErr, 0u);
+}
+
 __global__ void dispatch_recv_kernel(uint32_t *dflags, uint32_t *words,
                                      const int32_t *totals, int32_t *recv_count,
                                      int W, int check, uint32_t epoch,
@@ -748,6 +752,11 @@ cudaError_t launch_dispatch_recv(const Config &c, const Workspace &ws,
     dispatch_recv_kernel<<<1, threads, 0, st>>>(
         ws.dflags, ws.words, ws.group_base + (int64_t)c.Q * c.W, ws.recv_count,
         c.W, check_flags ? 1 : 0, epoch, c.timeout_ns);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_take_error(const Workspace &ws, cudaStream_t st) {
+    take_error_kernel<<<1, 1, 0, st>>>(ws.words);
     return cudaGetLastError();
 }
 

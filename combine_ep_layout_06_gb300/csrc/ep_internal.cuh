@@ -42,6 +42,7 @@ constexpr int kWordErr = 0;        // sticky device error word
 constexpr int kWordLayoutDone = 1; // "last CTA" ticket of the layout kernel
 constexpr int kWordSrcDone = 8;    // [W] per-source ticket of the dispatch copy
 constexpr int kWordMoeDone = 40;   // "last CTA" ticket of the grouping scan
+constexpr int kWordErrTaken = 41;  // the error word as ep_get_error last took it
 constexpr int kCounterWords = 64;  // 256 bytes
 
 struct Workspace {
@@ -153,6 +154,11 @@ cudaError_t launch_moe_ungroup(const Config &c, const Workspace &ws, const char 
 
 cudaError_t launch_identity_expert(const Config &c, const Workspace &ws,
                                    char *y, int64_t y_stride, cudaStream_t st);
+
+// Read and clear the error word in one atomic exchange (kWordErrTaken gets
+// the old value), so that a bit set meanwhile by work on another stream is
+// either taken now or left for the next call, never lost.
+cudaError_t launch_take_error(const Workspace &ws, cudaStream_t st);
 
 // Test harness: the FP8 quotient and scale identities over every bf16 pair.
 cudaError_t launch_fp8_quotient_check(unsigned long long *d_counts, cudaStream_t st);

@@ -46,6 +46,42 @@ __device__ __forceinline__ int chunk_start(const LayoutParams &p, int g, int r) 
            __ldcg(p.chunk_local + (int64_t)g * p.W + r);
 }
 
+// Per chunk g (one warp, lane = token of the chunk): the destination mask
+// of each token (all k ids loaded before the first is used, so a lane waits
+// for one memory latency rather than k in a row), written to masks; returns
+// in lane r (< W) the chunk's count for destination r (warp ballot).
+__device__ __forceinline__ int chunk_counts(const LayoutParams &p, int g, int lane) {
+    if (g >= p.G) return 0;
+    const int s = g / p.nch;
+    const int t = (g - s * p.nch) * kChunk + lane;
+    uint32_t mask = 0;
+    bool bad = false;
+    if (t < p.nt.n[s]) {
+        const int32_t *row = p.idx + ((int64_t)s * p.T + t) * p.k;
+        int32_t e[EP_MAX_TOPK];
+#pragma unroll
+        for (int j = 0; j < EP_MAX_TOPK; ++j)
+            if (j < p.k) e[j] = __ldg(row + j);
+#pragma unroll
+        for (int j = 0; j < EP_MAX_TOPK; ++j) {
+            if (j < p.k) {
+                if ((uint32_t)e[j] < (uint32_t)p.E)
+                    mask |= 1u << (e[j] / p.Er);
+                else
+                    bad = true;
+            }
+        }
+    }
+    if (bad) set_error(p.words, EP_DEVERR_BAD_INDEX);
+    if (t < p.T) p.masks[(int64_t)s * p.T + t] = mask;
+    int my_count = 0;
+    for (int r = 0; r < p.W; ++r) {
+        const uint32_t b = __ballot_sync(0xffffffffu, (mask >> r) & 1u);
+        if (lane == r) my_count = __popc(b);
+    }
+    return my_count;
+}
+
 __global__ void __launch_bounds__(kLayoutThreads)
 layout_kernel(const LayoutParams p) {
     __shared__ int s_cnt[kLayoutWarps][EP_MAX_WORLD];
@@ -62,38 +98,7 @@ layout_kernel(const LayoutParams p) {
     grid_dependents_may_launch();
 
     // ---- per chunk: masks and destination counts (warp ballot)
-    int my_count = 0;
-    if (g < p.G) {
-        const int s = g / p.nch;
-        const int t = (g - s * p.nch) * kChunk + lane;
-        uint32_t mask = 0;
-        bool bad = false;
-        if (t < p.nt.n[s]) {
-            // all k ids are loaded before the first is used, so the lane
-            // waits for one memory latency rather than k in a row
-            const int32_t *row = p.idx + ((int64_t)s * p.T + t) * p.k;
-            int32_t e[EP_MAX_TOPK];
-#pragma unroll
-            for (int j = 0; j < EP_MAX_TOPK; ++j)
-                if (j < p.k) e[j] = __ldg(row + j);
-#pragma unroll
-            for (int j = 0; j < EP_MAX_TOPK; ++j) {
-                if (j < p.k) {
-                    if ((uint32_t)e[j] < (uint32_t)p.E)
-                        mask |= 1u << (e[j] / p.Er);
-                    else
-                        bad = true;
-                }
-            }
-        }
-        if (bad) set_error(p.words, EP_DEVERR_BAD_INDEX);
-        if (t < p.T) p.masks[(int64_t)s * p.T + t] = mask;
-        for (int r = 0; r < p.W; ++r) {
-            const uint32_t b = __ballot_sync(0xffffffffu, (mask >> r) & 1u);
-            if (lane == r) my_count = __popc(b);
-        }
-    }
-    s_cnt[warp][lane] = my_count;
+    s_cnt[warp][lane] = chunk_counts(p, g, lane);
     __syncthreads();
 
     // ---- per group: prefix of each chunk inside the group, group totals
@@ -237,37 +242,8 @@ layout_cluster_kernel(const LayoutParams p) {
     grid_dependency_wait();
     grid_dependents_may_launch();
 
-    // ---- per chunk: masks and destination counts (as layout_kernel)
-    int my_count = 0;
-    if (g < p.G) {
-        const int s = g / p.nch;
-        const int t = (g - s * p.nch) * kChunk + lane;
-        uint32_t mask = 0;
-        bool bad = false;
-        if (t < p.nt.n[s]) {
-            const int32_t *row = p.idx + ((int64_t)s * p.T + t) * p.k;
-            int32_t e[EP_MAX_TOPK];
-#pragma unroll
-            for (int j = 0; j < EP_MAX_TOPK; ++j)
-                if (j < p.k) e[j] = __ldg(row + j);
-#pragma unroll
-            for (int j = 0; j < EP_MAX_TOPK; ++j) {
-                if (j < p.k) {
-                    if ((uint32_t)e[j] < (uint32_t)p.E)
-                        mask |= 1u << (e[j] / p.Er);
-                    else
-                        bad = true;
-                }
-            }
-        }
-        if (bad) set_error(p.words, EP_DEVERR_BAD_INDEX);
-        if (t < p.T) p.masks[(int64_t)s * p.T + t] = mask;
-        for (int r = 0; r < p.W; ++r) {
-            const uint32_t b = __ballot_sync(0xffffffffu, (mask >> r) & 1u);
-            if (lane == r) my_count = __popc(b);
-        }
-    }
-    s_cnt[warp][lane] = my_count;
+    // ---- per chunk: masks and destination counts
+    s_cnt[warp][lane] = chunk_counts(p, g, lane);
     __syncthreads();
     // chunk offsets inside the group (kept in s_cnt as exclusive prefixes)
     if (warp == 0 && lane < p.W) {

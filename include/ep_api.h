@@ -333,7 +333,8 @@ ep_status_t ep_moe_ungroup(ep_handle_t *h, const void *d_yg,
  * `stream` and forget the layout (combine then needs a new dispatch). */
 ep_status_t ep_reset(ep_handle_t *h, void *stream);
 
-/* Read and clear the device error word in `stream` order, then wait for
+/* Read and clear the device error word in `stream` order (one atomic
+ * exchange on the device, so no bit set concurrently is lost), then wait for
  * that stream alone (cudaStreamSynchronize; work on other streams keeps
  * running, and what it sets later shows in a later call).  *mask gets the
  * EP_DEVERR_* bits; the return is EP_SUCCESS for 0, else the status of the

@@ -393,6 +393,33 @@ def test_capacity_overflow_is_bounded_and_reported():
     _compare(wl, inp, res, cap)
 
 
+@pytest.mark.parametrize("name,fp8", [("dsv3", False), ("dsv3_fp8_zipf", True), ("ll_decode", False)])
+def test_receive_rows_past_the_count_are_untouched(name, fp8):
+    """Every byte of the workspace starts as a sentinel; after a dispatch the
+    receive rows at or past recv_count[r] (payload, scales, weights, ids,
+    src_pos) still hold it: the copy writes exactly the counted rows."""
+    wl = gen.WORKLOADS[name].scaled(96, hidden=1024)
+    wl = gen.dataclasses.replace(wl, fp8=fp8)
+    inp = gen.make_inputs(wl, num_tokens=gen.ragged_num_tokens(wl))
+    op = make_op(wl)
+    op.workspace.fill_(0xAB)
+    op.reset()
+    x, w, idx = to_device(inp)
+    op.dispatch(x, w, None, idx, num_tokens=[int(n) for n in inp.num_tokens])
+    torch.cuda.synchronize()
+    rc = op.recv_count.cpu().numpy()
+    assert int(rc.sum()) > 0
+    views = [op.out, op.out_w, op.out_idx, op.src_pos] + ([op.out_scales] if fp8 else [])
+    for r in range(wl.world_size):
+        n = int(rc[r])
+        for v in views:
+            tail = v[r, n:].contiguous().view(torch.uint8).cpu().numpy()
+            assert np.all(tail == 0xAB), (r, v.shape)
+            head = v[r, :n].contiguous().view(torch.uint8).cpu().numpy()
+            assert n == 0 or not np.all(head == 0xAB)
+    assert op.get_error() == (0, 0)
+
+
 def test_bad_expert_index_is_ignored_and_reported():
     wl = gen.WORKLOADS["tiny"]
     inp = gen.make_inputs(wl)
