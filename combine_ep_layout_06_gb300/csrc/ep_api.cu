@@ -278,12 +278,12 @@ static ep_status_t dispatch_send_impl(ep_handle_t *h, const void *d_x,
                                       bool publish, cudaStream_t st) {
     if (h->cfg.early_notify) ++h->dispatch_epoch;
     h->moe_valid = false;             // a grouping belongs to one dispatch
-    if (run_layout) {
+    // few chunks: the copy kernel computes the layout itself (no layout kernel)
+    const bool self_layout = run_layout && h->cfg.G <= self_layout_chunks();
+    if (run_layout && !self_layout) {
         const ep_status_t s =
             gpu(h, launch_layout(h->cfg, h->ws, d_idx, nt, st, publish), "layout");
         if (s != EP_SUCCESS) return s;
-        h->layout_valid = true;
-        h->layout_nt = nt;
     }
     DispatchArgs a;
     a.x = d_x;
@@ -292,8 +292,16 @@ static ep_status_t dispatch_send_impl(ep_handle_t *h, const void *d_x,
     a.idx = d_idx;
     a.nt = nt;
     a.epoch = h->dispatch_epoch;
-    a.after_layout = run_layout;
-    return gpu(h, launch_dispatch(h->cfg, h->ws, a, st), "dispatch");
+    a.after_layout = run_layout && !self_layout;
+    a.self_layout = self_layout;
+    a.publish = publish;
+    const ep_status_t s = gpu(h, launch_dispatch(h->cfg, h->ws, a, st), "dispatch");
+    if (s != EP_SUCCESS) return s;
+    if (run_layout) {
+        h->layout_valid = true;
+        h->layout_nt = nt;
+    }
+    return EP_SUCCESS;
 }
 
 ep_status_t ep_dispatch_send(ep_handle_t *h, const void *d_x, const float *d_w,

@@ -61,6 +61,9 @@ namespace {
 #ifndef EP_DISPATCH_PDL
 #define EP_DISPATCH_PDL 1              // launch the copy programmatically after the layout
 #endif
+#ifndef EP_DISPATCH_SELF_LAYOUT_CHUNKS
+#define EP_DISPATCH_SELF_LAYOUT_CHUNKS 8   // up to this many chunks the copy computes the layout
+#endif
 #ifndef EP_DISPATCH_REG_TPC
 #define EP_DISPATCH_REG_TPC 4          // tokens per CTA, register / FP8 path
 #endif
@@ -90,6 +93,12 @@ struct DispatchParams {
     uint32_t epoch;
     int64_t timeout_ns;
     TokenCounts nt;
+    // the whole layout computed by every CTA (G <= kSelfChunks); CTA 0 also
+    // writes the layout state that replay, the receive step and combine read
+    int self_layout;
+    int E, Er, G, publish;
+    uint32_t *masks_w;
+    int32_t *chunk_local_w, *group_tot_w, *group_base_w, *send_counts, *recv_count;
 };
 
 struct DispatchSmem {
@@ -104,11 +113,33 @@ struct BulkSmem {
     int32_t list[kChunk];
 };
 
-// Receive slots of the chunk's tokens (the within-chunk part of the layout):
-// warp 0 ballots each destination bit over the chunk's 32 tokens; a token's
-// slot on rank r is the chunk's start plus the number of lanes below it that
-// also go to r.  Fills spos / smask for all 32 tokens and writes pos for the
-// CTA's own tokens [i0, i0 + TPC).
+// Receive slots of a chunk's tokens (the within-chunk part of the layout),
+// one warp: lane l holds token t0 + l with destination mask m and, in lanes
+// r < W, the chunk's start my_base on rank r.  A token's slot on rank r is
+// the chunk's start plus the number of lanes below it that also go to r.
+// Fills spos / smask for all 32 tokens and writes pos for the CTA's own
+// tokens [i0, i0 + TPC).
+template <int TPC>
+__device__ __forceinline__ void slots_from(const DispatchParams &p, int s, int t0, int i0,
+                                           uint32_t m, int my_base,
+                                           int32_t (*spos)[EP_MAX_WORLD], uint32_t *smask) {
+    const int lane = threadIdx.x & 31;
+    const int t = t0 + lane;
+    const uint32_t below = lanemask_lt();
+    for (int r = 0; r < p.W; ++r) {
+        const uint32_t b = __ballot_sync(0xffffffffu, (m >> r) & 1u);
+        const int base = __shfl_sync(0xffffffffu, my_base, r);
+        spos[lane][r] = ((m >> r) & 1u) ? base + __popc(b & below) : -1;
+    }
+    smask[lane] = m;
+    if (t < p.T && lane >= i0 && lane < i0 + TPC) {
+        int32_t *dst = p.pos + ((int64_t)s * p.T + t) * p.W;
+        for (int r = 0; r < p.W; ++r) dst[r] = spos[lane][r];
+    }
+}
+
+// The same from the layout kernel's results (warp 0): the masks, and the
+// chunk's start = its group's base + its offset inside the group.
 template <int TPC>
 __device__ __forceinline__ void chunk_slots(const DispatchParams &p, int g, int s,
                                             int t0, int n_s, int i0,
@@ -120,16 +151,79 @@ __device__ __forceinline__ void chunk_slots(const DispatchParams &p, int g, int 
     const int my_base = (lane < p.W) ? p.group_base[(int64_t)(g / kGroup) * p.W + lane] +
                                            p.chunk_local[(int64_t)g * p.W + lane]
                                      : 0;
-    const uint32_t below = lanemask_lt();
-    for (int r = 0; r < p.W; ++r) {
-        const uint32_t b = __ballot_sync(0xffffffffu, (m >> r) & 1u);
-        const int base = __shfl_sync(0xffffffffu, my_base, r);
-        spos[lane][r] = ((m >> r) & 1u) ? base + __popc(b & below) : -1;
+    slots_from<TPC>(p, s, t0, i0, m, my_base, spos, smask);
+}
+
+// Up to kSelfChunks chunks (at most 256 tokens in all) every CTA computes
+// the whole layout itself -- one round of id loads, then ballots -- instead
+// of waiting for a layout kernel: the tiny workloads are pure latency, and
+// one kernel fewer is the larger part of their step.  Warps take chunks
+// c = warp, warp + kDispatchWarps, ...; CTA 0 writes the masks, chunk
+// offsets, group totals and bases (one group), send counts and recv_count.
+constexpr int kSelfChunks = EP_DISPATCH_SELF_LAYOUT_CHUNKS > 0 ? EP_DISPATCH_SELF_LAYOUT_CHUNKS : 1;
+static_assert(kSelfChunks <= kGroup, "the self layout covers one layout group");
+
+template <int TPC>
+__device__ void self_layout_slots(const DispatchParams &p, int g, int s, int t0, int i0,
+                                  int32_t (*spos)[EP_MAX_WORLD], uint32_t *smask,
+                                  int (*s_cnt)[EP_MAX_WORLD], uint32_t *s_own) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    for (int c = warp; c < p.G; c += kDispatchWarps) {
+        const int cs = c / p.nch;
+        const int t = (c - cs * p.nch) * kChunk + lane;
+        uint32_t mask = 0;
+        bool bad = false;
+        if (t < p.nt.n[cs]) {
+            const int32_t *row = p.idx + ((int64_t)cs * p.T + t) * p.k;
+            int32_t e[EP_MAX_TOPK];
+#pragma unroll
+            for (int j = 0; j < EP_MAX_TOPK; ++j)
+                if (j < p.k) e[j] = __ldg(row + j);
+#pragma unroll
+            for (int j = 0; j < EP_MAX_TOPK; ++j) {
+                if (j < p.k) {
+                    if ((uint32_t)e[j] < (uint32_t)p.E)
+                        mask |= 1u << (e[j] / p.Er);
+                    else
+                        bad = true;
+                }
+            }
+        }
+        if (blockIdx.x == 0) {
+            if (bad) set_error(p.words, EP_DEVERR_BAD_INDEX);
+            if (t < p.T) p.masks_w[(int64_t)cs * p.T + t] = mask;
+        }
+        int cnt = 0;
+        for (int r = 0; r < p.W; ++r) {
+            const uint32_t b = __ballot_sync(0xffffffffu, (mask >> r) & 1u);
+            if (lane == r) cnt = __popc(b);
+        }
+        s_cnt[c][lane] = cnt;
+        if (c == g) s_own[lane] = mask;
     }
-    smask[lane] = m;
-    if (t < p.T && lane >= i0 && lane < i0 + TPC) {
-        int32_t *dst = p.pos + ((int64_t)s * p.T + t) * p.W;
-        for (int r = 0; r < p.W; ++r) dst[r] = spos[lane][r];
+    __syncthreads();
+    if (warp == 0) {
+        int my_base = 0;
+        if (lane < p.W)
+            for (int c = 0; c < g; ++c) my_base += s_cnt[c][lane];
+        slots_from<TPC>(p, s, t0, i0, s_own[lane], my_base, spos, smask);
+    } else if (warp == 1 && blockIdx.x == 0 && lane < p.W) {
+        int run = 0;
+        for (int c = 0; c < p.G; ++c) {
+            p.chunk_local_w[(int64_t)c * p.W + lane] = run;
+            run += s_cnt[c][lane];
+        }
+        p.group_tot_w[lane] = run;
+        p.group_base_w[lane] = 0;
+        p.group_base_w[p.W + lane] = run;              // row Q = 1: the totals
+        if (run > p.cap) set_error(p.words, EP_DEVERR_CAPACITY);
+        if (p.publish) p.recv_count[lane] = run;
+        for (int sr = 0; sr < p.W; ++sr) {
+            int cnt = 0;
+            for (int c = sr * p.nch; c < (sr + 1) * p.nch; ++c) cnt += s_cnt[c][lane];
+            p.send_counts[sr * p.W + lane] = cnt;
+        }
     }
 }
 
@@ -344,7 +438,13 @@ dispatch_kernel(const DispatchParams p) {
     const int n_s = p.nt.n[s];
 
     grid_dependency_wait();
-    if (warp == 0) chunk_slots<TPC>(p, g, s, t0, n_s, i0, sm.pos, sm.mask);
+    if (p.self_layout) {
+        __shared__ int s_cnt[kSelfChunks][EP_MAX_WORLD];
+        __shared__ uint32_t s_own[kChunk];
+        self_layout_slots<TPC>(p, g, s, t0, i0, sm.pos, sm.mask, s_cnt, s_own);
+    } else if (warp == 0) {
+        chunk_slots<TPC>(p, g, s, t0, n_s, i0, sm.pos, sm.mask);
+    }
     __syncthreads();
 
     for (int i = i0 + warp; i < i0 + TPC; i += kDispatchWarps) {
@@ -506,7 +606,10 @@ dispatch_bulk_kernel(const DispatchParams p) {
 
     // The CTA's rows are its tokens below n_s.  Their loads do not depend on
     // the layout, so thread 0 issues them before waiting for it: launched
-    // programmatically after the layout kernel, they overlap its tail.
+    // programmatically after the layout kernel, they overlap its tail.  (The
+    // layout kernel waited for the kernel before it, so the rows are final.
+    // With the self layout no layout kernel runs, and the loads follow the
+    // wait instead.)
     const uint32_t bytes = (uint32_t)p.row_bytes;
     auto issue = [&](int j, uint64_t pol) {
         const int st = j % STAGES;
@@ -522,11 +625,24 @@ dispatch_bulk_kernel(const DispatchParams p) {
         s_n = n;
         for (int i = 0; i < STAGES; ++i) mbar_init(&bar[i], 1);
         mbar_init_fence();
-        const uint64_t pol = l2_evict_first_policy();
-        for (int j = 0; j < (n < STAGES ? n : STAGES); ++j) issue(j, pol);
+        if (!p.self_layout) {
+            const uint64_t pol = l2_evict_first_policy();
+            for (int j = 0; j < (n < STAGES ? n : STAGES); ++j) issue(j, pol);
+        }
     }
     grid_dependency_wait();
-    if (warp == 0) chunk_slots<TPC>(p, g, s, t0, n_s, i0, sm.pos, sm.mask);
+    if (p.self_layout) {
+        if (threadIdx.x == 0) {
+            const uint64_t pol = l2_evict_first_policy();
+            const int n0 = s_n;
+            for (int j = 0; j < (n0 < STAGES ? n0 : STAGES); ++j) issue(j, pol);
+        }
+        __shared__ int s_cnt[kSelfChunks][EP_MAX_WORLD];
+        __shared__ uint32_t s_own[kChunk];
+        self_layout_slots<TPC>(p, g, s, t0, i0, sm.pos, sm.mask, s_cnt, s_own);
+    } else if (warp == 0) {
+        chunk_slots<TPC>(p, g, s, t0, n_s, i0, sm.pos, sm.mask);
+    }
     __syncthreads();
     const int n = s_n;
 
@@ -732,7 +848,18 @@ cudaError_t launch_dispatch(const Config &c, const Workspace &ws,
     p.epoch = a.epoch;
     p.timeout_ns = c.timeout_ns;
     p.nt = a.nt;
-    const bool pdl = a.after_layout && EP_DISPATCH_PDL;
+    p.self_layout = a.self_layout ? 1 : 0;
+    p.E = c.E; p.Er = c.Er; p.G = c.G;
+    p.publish = a.publish ? 1 : 0;
+    p.masks_w = ws.masks;
+    p.chunk_local_w = ws.chunk_local;
+    p.group_tot_w = ws.group_tot;
+    p.group_base_w = ws.group_base;
+    p.send_counts = ws.send_counts;
+    p.recv_count = ws.recv_count;
+    // the self-layout copy is the step's first kernel: launched programmatically
+    // after whatever precedes it, it waits for that kernel before any read
+    const bool pdl = (a.after_layout || a.self_layout) && EP_DISPATCH_PDL;
     if (c.fp8 && !a.scales_in)      // fused quantisation
         return launch_dispatch_t<true, EP_DISPATCH_FP8_UNROLL, EP_DISPATCH_REG_TPC>(c, p, pdl, st);
     // rows copied unchanged: bf16, or pre-quantised codes (H <= 16384 bytes)
@@ -754,6 +881,8 @@ cudaError_t launch_dispatch_recv(const Config &c, const Workspace &ws,
         c.W, check_flags ? 1 : 0, epoch, c.timeout_ns);
     return cudaGetLastError();
 }
+
+int self_layout_chunks() { return EP_DISPATCH_SELF_LAYOUT_CHUNKS; }
 
 cudaError_t launch_take_error(const Workspace &ws, cudaStream_t st) {
     take_error_kernel<<<1, 1, 0, st>>>(ws.words);

@@ -113,7 +113,12 @@ struct DispatchArgs {
     TokenCounts nt;
     uint32_t epoch;        // flag value when early_notify
     bool after_layout;     // launched right after the layout kernel on the same stream
+    bool self_layout;      // no layout kernel: the copy computes the layout (few chunks)
+    bool publish;          // with self_layout: also write recv_count
 };
+
+// Chunks (W * ceil(T/32)) up to which the copy computes the layout itself.
+int self_layout_chunks();
 cudaError_t launch_dispatch(const Config &c, const Workspace &ws,
                             const DispatchArgs &a, cudaStream_t st);
 
