@@ -48,6 +48,7 @@ METRIC = "dispatch+combine tokens/s and HBM GB/s (% of GB300 peak), 1 GPU"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 WORKLOAD = "dsv3"
+SELF_LAYOUT_CHUNKS = 8     # the library launches no layout kernel up to this many chunks
 
 
 def parse():
@@ -423,10 +424,14 @@ class Case:
                 else "dispatch_bulk_kernel")
 
     def launches_per_step(self):
-        # this library's kernels per timed step: layout, copy, combine (the
-        # receive phase launches none without early notification), plus the
-        # scatter send in scatter mode
-        return 3 + (1 if self.combine_mode == "scatter" else 0)
+        # this library's kernels per timed step: layout (none when the routing
+        # spans at most SELF_LAYOUT_CHUNKS 32-token chunks: the copy computes
+        # it), copy, combine (the receive phase launches none without early
+        # notification), plus the scatter send in scatter mode
+        wl = self.wl
+        chunks = wl.world_size * -(-wl.max_tokens_per_rank // 32)
+        return (2 + (1 if chunks > SELF_LAYOUT_CHUNKS else 0) +
+                (1 if self.combine_mode == "scatter" else 0))
 
     def close(self):
         import torch

@@ -38,7 +38,7 @@ def test_bench_line_keys_on_a_small_workload():
     e = d["e2e"]
     assert e["value"] > 0 and e["output_check"] == "pass"
     assert e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
-    assert d["gpu_launches"] == 3 * 5
+    assert d["gpu_launches"] == 2 * 5          # tiny: copy (with the layout) + combine
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
     assert d["identity_check"] == "pass" and d["device_errors"] == 0
     # every workload of the benchmark, measured in the same run
