@@ -213,8 +213,11 @@ ep_status_t ep_layout(ep_handle_t *h, const int32_t *d_idx,
  * Inputs must stay unchanged until the receive phase has been enqueued.
  * The copy kernel is launched as a programmatic dependent of the layout
  * kernel just before it (both enqueued by this call), so stream capture
- * records a programmatic edge between them; anything enqueued earlier on
- * the stream is complete before either starts. */
+ * records a programmatic edge between them.  When the routing spans at most
+ * 8 chunks of 32 tokens (W * ceil(T/32) <= 8), no layout kernel runs: the
+ * copy computes the layout itself and is launched as a programmatic
+ * dependent of whatever kernel precedes it.  Either way anything enqueued
+ * earlier on the stream is complete before the first read of the inputs. */
 ep_status_t ep_dispatch_send(ep_handle_t *h, const void *d_x, const float *d_w,
                              const float *d_scales, const int32_t *d_idx,
                              const int32_t *h_num_tokens, void *stream);
