@@ -267,6 +267,43 @@ def test_routing_replay_after_one_call_dispatch():
         assert np.array_equal(out[r, :n], ref["out"][r, :n])
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_routing_replay_after_a_dispatch_that_computed_its_own_layout(fp8):
+    """At most 8 chunks of 32 tokens the copy kernel computes the layout
+    itself, and its CTA 0 writes the layout state (masks, chunk offsets,
+    group bases, send counts, recv_count) that routing replay, the receive
+    step and combine read: a replay with new rows and an early-notification
+    receive must then give the oracle's results."""
+    wl = gen.Workload("self", 4, 16, 3, 60, 256, fp8=fp8)       # 4 x 2 = 8 chunks
+    inp = gen.make_inputs(wl, num_tokens=[60, 33, 0, 51])
+    for kw in (dict(), dict(early_notify=True)):
+        op = make_op(wl, **kw)
+        x, w, idx = to_device(inp)
+        nt = [int(n) for n in inp.num_tokens]
+        op.dispatch(x, w, None, idx, num_tokens=nt)
+        x2 = torch.randn_like(x, dtype=torch.float32).to(torch.bfloat16)
+        op.dispatch_send_replay(x2, w, idx, num_tokens=nt)
+        op.dispatch_recv()
+        op.identity_expert()
+        out, out_w = op.combine(weights=op.out_w, indices=idx)
+        torch.cuda.synchronize()
+        inp2 = gen.Inputs(wl, bits(x2).reshape(inp.x_bits.shape), inp.weights,
+                          inp.indices, inp.num_tokens)
+        ref = oracle.run_all(inp2, cap=op.cap)
+        assert np.array_equal(op.recv_count.cpu().numpy(), ref["recv_count"])
+        assert np.array_equal(op.send_counts.cpu().numpy(), ref["C"])
+        assert np.array_equal(op.pos.cpu().numpy(), ref["pos"])
+        got_out = bits(op.out)
+        for r in range(wl.world_size):
+            n = int(ref["recv_count"][r])
+            assert np.array_equal(got_out[r, :n], ref["out"][r, :n]), r
+        got = bits(out)
+        for s_ in range(wl.world_size):
+            n = int(inp.num_tokens[s_])
+            assert np.array_equal(got[s_, :n], ref["combined"][s_, :n]), s_
+        assert op.get_error() == (0, 0)
+
+
 @pytest.mark.parametrize("name,fp8", [("ll_decode", False), ("dsv3", False), ("dsv3", True)])
 def test_captured_graph_replayed_on_new_routing(name, fp8):
     """A captured one-call dispatch + combine replayed after the inputs were
